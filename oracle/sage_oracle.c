@@ -1,0 +1,344 @@
+/*
+ * sage_oracle.c -- CPU oracle for SageAttention-style quantized attention.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the slow, plain, obviously-correct
+ * statement of what the quantize-then-attend path computes.  Only the test
+ * suite, the smoke check and the benchmark's CPU-baseline leg may load it.
+ * It shares no code, header, table or constant generator with the CUDA path.
+ *
+ * Sources (web pages describing the method):
+ *  [I15014]  diffusers issue #15014 "gfx1201 (RDNA4) SageAttention attention
+ *            backend: aiter package or Hub kernel?", section "Is your feature
+ *            request related to a problem?" (kernel contract bullets):
+ *            INT8 QK^T and FP8 PV with FP32 accumulation; Q/K quantized per
+ *            32-row block, V per channel; BF16 [B, S, H, 128], equal Q/K/V
+ *            shapes, no mask, non-causal.
+ *  [P15060]  diffusers PR #15060 "Add aiter_sage_hub attention backend for AMD
+ *            RDNA4 (gfx1201)", section "What does this PR do?": INT8 QK^T,
+ *            FP8 PV, head dim 128, the kernel returns no LSE.
+ *
+ * Readings of points the pages leave open (each one is fixed here once):
+ *  R1  one FP32 scale per 32 consecutive tokens of one (batch, head); blocks
+ *      start at token 0 and never cross heads; the last block may be short.
+ *  R2  Q/K symmetric INT8: scale = amax / 127 (fp32 division, RNE),
+ *      code = clamp(rint(x / scale), -127, 127) with x / scale an fp32 RNE
+ *      division; an all-zero block has scale 0 and codes 0.
+ *  R3  FP8 is OCP E4M3FN (bias 7, max 448, subnormal quantum 2^-9, no Inf);
+ *      conversion is round-to-nearest-even with saturation to +-448.
+ *  R4  V per channel = per (batch, head, d) over all S tokens;
+ *      sv = amax / 448, code = e4m3(v / sv); an all-zero channel has sv = 0.
+ *  R5  QK^T: integer products summed exactly.  |acc| <= 128 * 127^2 < 2^24,
+ *      so FP32 accumulation of these products is exact too and equals INT32.
+ *  R6  score s = ((float)acc * (sq * sk)) * softmax_scale, fp32, left to right.
+ *  R7  softmax in FP32, two-pass: m = max_j s_j, p_j = fp32(exp(s_j - m))
+ *      with s_j - m an fp32 subtraction and exp evaluated in double then
+ *      rounded once to fp32.
+ *  R8  P to FP8: code_j = e4m3(p_j * 448) (fp32 product).
+ *  R9  normaliser L = sum_j dec(code_j) (the applied quantised weights);
+ *      l_mode = 1 selects the alternative L = sum_j 448 * p_j.
+ *  R10 PV: O[d] = sum_j dec(pcode_j) * dec(vcode_jd).  Every product is a
+ *      multiple of 2^-18 below 2^18 and there are at most 2^16 terms, so the
+ *      double sum is exact and order-independent.
+ *  R11 out[d] = bf16_rne((float)(O[d] * sv[d] / L)), layout [B, S, H, D].
+ *
+ * Build: gcc -O2 -fopenmp -ffp-contract=off -fno-fast-math -shared -fPIC
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ---------------------------------------------------------------- BF16 -- */
+
+static float bf16_to_f32(uint16_t h) {
+    uint32_t u = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+/* Round an fp32 value to the nearest bf16, ties to even (NaN kept quiet). */
+static uint16_t f32_to_bf16_rne(float f) {
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    if ((u & 0x7f800000u) == 0x7f800000u && (u & 0x007fffffu) != 0)
+        return (uint16_t)((u >> 16) | 0x0040u);
+    uint32_t lsb = (u >> 16) & 1u;
+    return (uint16_t)((u + 0x7fffu + lsb) >> 16);
+}
+
+/* ------------------------------------------------------------ E4M3FN -- */
+
+/* Value of an E4M3FN code: (-1)^s * 2^(e-7) * (1 + m/8) for e > 0,
+ * (-1)^s * 2^-6 * (m/8) for e == 0; e == 15 && m == 7 is NaN. */
+double oracle_e4m3_decode(uint8_t c) {
+    int s = (c >> 7) & 1, e = (c >> 3) & 15, m = c & 7;
+    double mag;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0) mag = ldexp((double)m, -9);
+    else mag = ldexp(1.0 + m / 8.0, e - 7);
+    return s ? -mag : mag;
+}
+
+/* Round y to E4M3FN, nearest-even, saturating to +-448 (R3).  The grid step
+ * in the binade [2^e, 2^(e+1)) is 2^(e-3); below 2^-6 the step is 2^-9. */
+uint8_t oracle_e4m3_encode(float y) {
+    if (isnan(y)) return 0x7f;
+    uint8_t sign = signbit(y) ? 0x80 : 0x00;
+    double a = fabs((double)y);
+    if (a >= 448.0) return sign | 0x7e;
+    int e;
+    if (a == 0.0) return sign;
+    (void)frexp(a, &e);          /* a = f * 2^e, f in [0.5, 1) */
+    e -= 1;                      /* floor(log2 a) */
+    if (e < -6) e = -6;
+    double quantum = ldexp(1.0, e - 3);
+    double r = nearbyint(a / quantum) * quantum;   /* a/quantum is exact */
+    if (r > 448.0) r = 448.0;
+    if (r == 0.0) return sign;
+    if (r < ldexp(1.0, -6))      /* subnormal: r = m * 2^-9, m in 1..7 */
+        return sign | (uint8_t)(r / ldexp(1.0, -9));
+    int er;
+    (void)frexp(r, &er);
+    er -= 1;                     /* rounding may have moved r up one binade */
+    int mant = (int)(r / ldexp(1.0, er) * 8.0) - 8;
+    return sign | (uint8_t)(((er + 7) << 3) | mant);
+}
+
+/* ------------------------------------------------- Q/K quantisation -- */
+
+/* x: bf16 [B, S, H, D].  codes: int8 [B, H, S_pad, D] (rows >= S are 0).
+ * scale: fp32 [B, H, nb], nb = ceil(S / 32).  [I15014] bullet 1; R1, R2. */
+void oracle_quantize_qk(const uint16_t *x, int B, int S, int H, int D,
+                        int S_pad, int8_t *codes, float *scale) {
+    int nb = (S + 31) / 32;
+#pragma omp parallel for collapse(2) schedule(static)
+    for (int b = 0; b < B; ++b)
+        for (int h = 0; h < H; ++h) {
+            int8_t *dst = codes + ((size_t)b * H + h) * S_pad * D;
+            memset(dst, 0, (size_t)S_pad * D);
+            for (int blk = 0; blk < nb; ++blk) {
+                int r0 = blk * 32, r1 = r0 + 32 < S ? r0 + 32 : S;
+                float amax = 0.0f;
+                for (int s = r0; s < r1; ++s)
+                    for (int d = 0; d < D; ++d) {
+                        float v = fabsf(bf16_to_f32(x[(((size_t)b * S + s) * H + h) * D + d]));
+                        if (v > amax) amax = v;
+                    }
+                float sc = amax / 127.0f;
+                scale[((size_t)b * H + h) * nb + blk] = sc;
+                if (sc == 0.0f) continue;
+                for (int s = r0; s < r1; ++s)
+                    for (int d = 0; d < D; ++d) {
+                        float v = bf16_to_f32(x[(((size_t)b * S + s) * H + h) * D + d]);
+                        float r = rintf(v / sc);
+                        if (r > 127.0f) r = 127.0f;
+                        if (r < -127.0f) r = -127.0f;
+                        dst[(size_t)s * D + d] = (int8_t)r;
+                    }
+            }
+        }
+}
+
+/* ---------------------------------------------------- V quantisation -- */
+
+/* v: bf16 [B, S, H, D].  vt: e4m3 [B, H, D, S_pad] (V transposed, columns
+ * >= S are 0).  vscale: fp32 [B, H, D].  [I15014] bullet 1 ("V per
+ * channel"), [P15060] ("FP8 PV"); R3, R4. */
+void oracle_quantize_v(const uint16_t *v, int B, int S, int H, int D,
+                       int S_pad, uint8_t *vt, float *vscale) {
+#pragma omp parallel for collapse(3) schedule(static)
+    for (int b = 0; b < B; ++b)
+        for (int h = 0; h < H; ++h)
+            for (int d = 0; d < D; ++d) {
+                uint8_t *dst = vt + (((size_t)b * H + h) * D + d) * S_pad;
+                memset(dst, 0, (size_t)S_pad);
+                float amax = 0.0f;
+                for (int s = 0; s < S; ++s) {
+                    float a = fabsf(bf16_to_f32(v[(((size_t)b * S + s) * H + h) * D + d]));
+                    if (a > amax) amax = a;
+                }
+                float sv = amax / 448.0f;
+                vscale[((size_t)b * H + h) * D + d] = sv;
+                if (sv == 0.0f) continue;
+                for (int s = 0; s < S; ++s) {
+                    float x = bf16_to_f32(v[(((size_t)b * S + s) * H + h) * D + d]);
+                    dst[s] = oracle_e4m3_encode(x / sv);
+                }
+            }
+}
+
+/* ------------------------------------------------------------ QK^T -- */
+
+/* Exact integer Q K^T for every (b, h): s_out int32 [B, H, S, S].
+ * Returns 0, or -1 if a sum does not fit int32 (cannot happen for codes in
+ * [-127, 127] and D <= 128).  R5. */
+int oracle_qk_int32(const int8_t *q, const int8_t *k, int B, int S, int H,
+                    int D, int S_pad, int32_t *s_out) {
+    int bad = 0;
+#pragma omp parallel for collapse(3) schedule(static) reduction(| : bad)
+    for (int b = 0; b < B; ++b)
+        for (int h = 0; h < H; ++h)
+            for (int i = 0; i < S; ++i) {
+                const int8_t *qi = q + (((size_t)b * H + h) * S_pad + i) * D;
+                for (int j = 0; j < S; ++j) {
+                    const int8_t *kj = k + (((size_t)b * H + h) * S_pad + j) * D;
+                    int64_t acc = 0;
+                    for (int c = 0; c < D; ++c) acc += (int64_t)qi[c] * kj[c];
+                    if (acc > INT32_MAX || acc < INT32_MIN) bad = 1;
+                    s_out[(((size_t)b * H + h) * S + i) * S + j] = (int32_t)acc;
+                }
+            }
+    return bad ? -1 : 0;
+}
+
+/* ------------------------------------------------------- attention -- */
+
+/* One query row (b, h, i).  Writes D bf16 outputs to out_row.  If pcodes is
+ * not NULL it receives the S FP8 codes of P and *L_out the normaliser.
+ * vdec is this head's decoded V, [S][D] floats (exact).  R6..R11. */
+static void attend_row(const int8_t *q, const float *qs, const int8_t *k,
+                       const float *ks, const float *vdec, const float *vs,
+                       int b, int h, int i, int S, int H, int D, int S_pad,
+                       float softmax_scale, int l_mode, float *sbuf,
+                       uint8_t *cbuf, double *obuf, uint16_t *out_row,
+                       uint8_t *pcodes, double *L_out) {
+    int nb = (S + 31) / 32;
+    const int8_t *qi = q + (((size_t)b * H + h) * S_pad + i) * D;
+    float sq = qs[((size_t)b * H + h) * nb + i / 32];
+    /* scores (R5, R6) */
+    float m = -INFINITY;
+    for (int j = 0; j < S; ++j) {
+        const int8_t *kj = k + (((size_t)b * H + h) * S_pad + j) * D;
+        int32_t acc = 0;
+        for (int c = 0; c < D; ++c) acc += (int32_t)qi[c] * (int32_t)kj[c];
+        float sk = ks[((size_t)b * H + h) * nb + j / 32];
+        float s = ((float)acc * (sq * sk)) * softmax_scale;
+        sbuf[j] = s;
+        if (s > m) m = s;
+    }
+    /* probabilities, FP8 codes, normaliser (R7, R8, R9) */
+    double L = 0.0;
+    for (int j = 0; j < S; ++j) {
+        float t = sbuf[j] - m;
+        float p = (float)exp((double)t);
+        uint8_t c = oracle_e4m3_encode(p * 448.0f);
+        cbuf[j] = c;
+        L += l_mode ? 448.0 * (double)p : oracle_e4m3_decode(c);
+    }
+    /* PV with exact products and exact double sums (R10) */
+    for (int d = 0; d < D; ++d) obuf[d] = 0.0;
+    for (int j = 0; j < S; ++j) {
+        double w = oracle_e4m3_decode(cbuf[j]);
+        if (w == 0.0) continue;
+        const float *vj = vdec + (size_t)j * D;
+        for (int d = 0; d < D; ++d) obuf[d] += w * (double)vj[d];
+    }
+    /* epilogue (R11) */
+    for (int d = 0; d < D; ++d) {
+        double o = obuf[d] * (double)vs[((size_t)b * H + h) * D + d] / L;
+        out_row[d] = f32_to_bf16_rne((float)o);
+    }
+    if (pcodes) memcpy(pcodes, cbuf, (size_t)S);
+    if (L_out) *L_out = L;
+}
+
+/* Decode one head's V^T codes into [S][D] floats (e4m3 values are exact in
+ * fp32). */
+static void decode_v_head(const uint8_t *vt, int b, int h, int S, int H, int D,
+                          int S_pad, float *vdec) {
+    for (int d = 0; d < D; ++d) {
+        const uint8_t *row = vt + (((size_t)b * H + h) * D + d) * S_pad;
+        for (int s = 0; s < S; ++s) vdec[(size_t)s * D + d] = (float)oracle_e4m3_decode(row[s]);
+    }
+}
+
+/* Attention output for a list of query rows.  rows: n triples (b, h, i).
+ * out: bf16 [n, D] in the order of rows.  Every (b, h) named in rows must
+ * appear; heads are decoded once.  Returns 0, or -1 on allocation failure.
+ * [I15014] bullets 1-2, [P15060] ("no LSE"): the output is the normalised
+ * attention only. */
+int oracle_attend_rows(const int8_t *q, const float *qs, const int8_t *k,
+                       const float *ks, const uint8_t *vt, const float *vs,
+                       int B, int S, int H, int D, int S_pad,
+                       float softmax_scale, int l_mode, const int32_t *rows,
+                       int64_t n, uint16_t *out) {
+    /* decode the heads in use */
+    int nheads = B * H;
+    float **vdec = (float **)calloc((size_t)nheads, sizeof(float *));
+    if (!vdec) return -1;
+    int fail = 0;
+    for (int64_t r = 0; r < n; ++r) {
+        int bh = rows[3 * r] * H + rows[3 * r + 1];
+        if (!vdec[bh]) {
+            vdec[bh] = (float *)malloc((size_t)S * D * sizeof(float));
+            if (!vdec[bh]) { fail = 1; break; }
+        }
+    }
+    if (!fail) {
+#pragma omp parallel for schedule(static)
+        for (int bh = 0; bh < nheads; ++bh)
+            if (vdec[bh]) decode_v_head(vt, bh / H, bh % H, S, H, D, S_pad, vdec[bh]);
+#pragma omp parallel
+        {
+            float *sbuf = (float *)malloc((size_t)S * sizeof(float));
+            uint8_t *cbuf = (uint8_t *)malloc((size_t)S);
+            double *obuf = (double *)malloc((size_t)D * sizeof(double));
+            if (!sbuf || !cbuf || !obuf) {
+#pragma omp atomic write
+                fail = 1;
+            } else {
+#pragma omp for schedule(dynamic, 4)
+                for (int64_t r = 0; r < n; ++r) {
+                    int b = rows[3 * r], h = rows[3 * r + 1], i = rows[3 * r + 2];
+                    attend_row(q, qs, k, ks, vdec[b * H + h], vs, b, h, i, S, H, D,
+                               S_pad, softmax_scale, l_mode, sbuf, cbuf, obuf,
+                               out + (size_t)r * D, NULL, NULL);
+                }
+            }
+            free(sbuf); free(cbuf); free(obuf);
+        }
+    }
+    for (int bh = 0; bh < nheads; ++bh) free(vdec[bh]);
+    free(vdec);
+    return fail ? -1 : 0;
+}
+
+/* Single row with its FP8 P codes and normaliser exposed (for the pins on
+ * the softmax/normaliser readings R7-R9). */
+int oracle_attend_row_debug(const int8_t *q, const float *qs, const int8_t *k,
+                            const float *ks, const uint8_t *vt, const float *vs,
+                            int B, int S, int H, int D, int S_pad,
+                            float softmax_scale, int l_mode, int b, int h, int i,
+                            uint16_t *out_row, uint8_t *pcodes, double *L_out) {
+    (void)B;
+    float *vdec = (float *)malloc((size_t)S * D * sizeof(float));
+    float *sbuf = (float *)malloc((size_t)S * sizeof(float));
+    uint8_t *cbuf = (uint8_t *)malloc((size_t)S);
+    double *obuf = (double *)malloc((size_t)D * sizeof(double));
+    int rc = -1;
+    if (vdec && sbuf && cbuf && obuf) {
+        decode_v_head(vt, b, h, S, H, D, S_pad, vdec);
+        attend_row(q, qs, k, ks, vdec, vs, b, h, i, S, H, D, S_pad, softmax_scale,
+                   l_mode, sbuf, cbuf, obuf, out_row, pcodes, L_out);
+        rc = 0;
+    }
+    free(vdec); free(sbuf); free(cbuf); free(obuf);
+    return rc;
+}
+
+/* Threads the OpenMP runtime will use (for the benchmark's core count). */
+#ifdef _OPENMP
+#include <omp.h>
+int oracle_num_threads(void) { return omp_get_max_threads(); }
+#else
+int oracle_num_threads(void) { return 1; }
+#endif
+
+/* Element-wise E4M3FN conversion over arrays (for the format pins). */
+void oracle_e4m3_encode_array(const float *y, int64_t n, uint8_t *out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_e4m3_encode(y[i]);
+}
+void oracle_e4m3_decode_array(const uint8_t *c, int64_t n, double *out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_e4m3_decode(c[i]);
+}

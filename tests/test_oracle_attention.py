@@ -1,0 +1,225 @@
+"""Pins for the oracle's attention (scores, FP32 softmax, FP8 P, PV, epilogue)
+and for the float64 unquantized reference.
+
+Sources: diffusers issue #15014, kernel contract bullets (INT8 QK^T, FP8 PV,
+FP32 accumulation; BF16 [B, S, H, 128]; no mask, non-causal); diffusers PR
+#15060, "What does this PR do?" (no LSE) and its review thread (the real
+kernel reaches cosine 0.9993 against SDPA at head dim 128).  The readings R6-R11
+are listed in the oracle's header.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from quantized_attention_diffusion_gb300.workloads import (WORKLOADS, bf16_bits, make_qkv,
+                                                          make_workload)
+
+
+def bf16(x):
+    return bf16_bits(torch.tensor(np.asarray(x, dtype=np.float32)).to(torch.bfloat16))
+
+
+def f32(bits):
+    return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+def cosine(a, b):
+    a = np.asarray(a, dtype=np.float64).ravel()
+    b = np.asarray(b, dtype=np.float64).ravel()
+    return float(a @ b / (np.linalg.norm(a) * np.linalg.norm(b)))
+
+
+def golden(name):
+    import os
+    path = os.path.join(os.path.dirname(__file__), "golden", "pages_accuracy.txt")
+    for line in open(path):
+        if line.startswith("#") or not line.strip():
+            continue
+        fields = [f.strip() for f in line.split("|")]
+        if fields[0] == name:
+            return float(fields[1])
+    raise KeyError(name)
+
+
+def qkv_bits(B, S, H, seed, recipe="normal"):
+    return [bf16_bits(t) for t in make_qkv(B, S, H, recipe=recipe, seed=seed)]
+
+
+# ------------------------------------------------------ worked example --
+
+def test_two_token_worked_example():
+    """Hand-derived example (every step exact or one rounding).
+
+    Q rows (channel 0 only) 127 and 63, K rows 127 and 63: one block, scale
+    127/127 = 1, codes equal the values.  softmax_scale = 2^-11 makes the
+    scores exact: row 0 s = (16129, 8001) / 2048, row 1 s = (8001, 3969) / 2048.
+    Row 0: p = (1, exp(-3.96875) = 0.018897) -> P codes 448 and 8.4659 -> 8,
+    L = 456.  Row 1: p = (1, exp(-1.96875) = 0.139631) -> 448 and 62.55 -> 64
+    (grid step 4 in [32, 64)), L = 512.  V channel d is +2^(d%4) at token 0
+    and -2^(d%4) at token 1: codes +-448, sv = 2^(d%4)/448.
+    out row 0 = (448-8)/456 * 2^(d%4) = 0.96491 -> bf16 0.96484375 * 2^(d%4);
+    out row 1 = (448-64)/512 * 2^(d%4) = 0.75 * 2^(d%4).
+    With L taken from the unquantised p instead (l_mode 1) row 1 becomes
+    384/510.55 = 0.75212 -> bf16 0.75390625, which tells the readings apart.
+    """
+    D = 128
+    q = np.zeros((1, 2, 1, D), np.float32)
+    k = np.zeros((1, 2, 1, D), np.float32)
+    v = np.zeros((1, 2, 1, D), np.float32)
+    q[0, :, 0, 0] = [127.0, 63.0]
+    k[0, :, 0, 0] = [127.0, 63.0]
+    pw = 2.0 ** (np.arange(D) % 4)
+    v[0, 0, 0, :] = pw
+    v[0, 1, 0, :] = -pw
+    quant = oracle.quantize(bf16(q), bf16(k), bf16(v))
+    qc, qs, kc, ks, vt, vs = quant
+    assert qs[0, 0, 0] == 1.0 and ks[0, 0, 0] == 1.0
+    assert np.all(vt[0, 0, :, 0] == 0x7E) and np.all(vt[0, 0, :, 1] == 0xFE)
+    scale = 2.0 ** -11
+    out0, p0, L0 = oracle.attend_row_debug(quant, 2, scale, 0, 0, 0)
+    out1, p1, L1 = oracle.attend_row_debug(quant, 2, scale, 0, 0, 1)
+    assert list(oracle.e4m3_decode(p0)) == [448.0, 8.0] and L0 == 456.0
+    assert list(oracle.e4m3_decode(p1)) == [448.0, 64.0] and L1 == 512.0
+    assert np.array_equal(f32(out0), (0.96484375 * pw).astype(np.float32))
+    assert np.array_equal(f32(out1), (0.75 * pw).astype(np.float32))
+    alt1, _, Lalt = oracle.attend_row_debug(quant, 2, scale, 0, 0, 1, l_mode=1)
+    assert abs(Lalt - 448 * (1 + math.exp(-1.96875))) < 1e-4
+    assert np.array_equal(f32(alt1), (0.75390625 * pw).astype(np.float32))
+
+
+# ----------------------------------------------------------- invariants --
+
+def test_constant_v_gives_constant_output():
+    B, S, H = 1, 200, 2
+    q, k, _ = qkv_bits(B, S, H, seed=11, recipe="k_channel_offset")
+    rng = np.random.default_rng(11)
+    c = rng.normal(0, 3, size=(H, 128)).astype(np.float32)
+    c[0, :4] = [3500.0, -3500.0, 1e-3, 0.0]        # the pages' V ~ 3500 head, tiny, zero
+    v = bf16(np.broadcast_to(c[None, None], (B, S, H, 128)))
+    out = oracle.attention(q, k, v, 1 / math.sqrt(128))
+    expect = np.broadcast_to(v[:, :1], out.shape)
+    assert np.array_equal(out, expect)
+
+
+def test_single_token_returns_v():
+    q, k, v = qkv_bits(2, 1, 3, seed=12)
+    out = oracle.attention(q, k, v, 1 / math.sqrt(128))
+    assert np.array_equal(out, v)
+
+
+def test_equal_keys_give_mean_of_dequantised_v():
+    B, S, H = 1, 20, 1
+    q, k, v = qkv_bits(B, S, H, seed=13)
+    k = np.broadcast_to(k[:, :1], k.shape).copy()
+    out = oracle.attention(q, k, v, 1 / math.sqrt(128))
+    vt, vs = oracle.quantize_v(v)
+    mean = oracle.e4m3_decode(vt[0, 0, :, :S]).sum(axis=1) * vs[0, 0].astype(np.float64) / S
+    expect = bf16(mean.astype(np.float32))
+    assert np.array_equal(out[0, :, 0, :], np.broadcast_to(expect, (S, 128)))
+
+
+def _block_preserving_permutation(S, rng):
+    nb = S // 32
+    blocks = rng.permutation(nb)
+    return np.concatenate([32 * b + rng.permutation(32) for b in blocks])
+
+
+def test_kv_permutation_within_and_across_whole_blocks_is_exact():
+    B, S, H = 1, 256, 2
+    q, k, v = qkv_bits(B, S, H, seed=14, recipe="k_channel_offset")
+    base = oracle.attention(q, k, v, 1 / math.sqrt(128))
+    perm = _block_preserving_permutation(S, np.random.default_rng(14))
+    out = oracle.attention(q, k[:, perm], v[:, perm], 1 / math.sqrt(128))
+    assert np.array_equal(out, base)
+
+
+def test_kv_arbitrary_permutation_within_tolerance():
+    B, S, H = 1, 256, 2
+    q, k, v = qkv_bits(B, S, H, seed=15)
+    base = f32(oracle.attention(q, k, v, 1 / math.sqrt(128)))
+    perm = np.random.default_rng(15).permutation(S)
+    out = f32(oracle.attention(q, k[:, perm], v[:, perm], 1 / math.sqrt(128)))
+    assert np.abs(out - base).max() <= 2e-2
+    assert not np.array_equal(out, base)          # K block scales did move
+
+
+def test_query_permutation_within_block_permutes_rows():
+    B, S, H = 1, 96, 1
+    q, k, v = qkv_bits(B, S, H, seed=16)
+    base = oracle.attention(q, k, v, 1 / math.sqrt(128))
+    perm = _block_preserving_permutation(S, np.random.default_rng(16))
+    out = oracle.attention(q[:, perm], k, v, 1 / math.sqrt(128))
+    assert np.array_equal(out, base[:, perm])
+
+
+def test_heads_and_batches_are_independent():
+    B, S, H = 2, 100, 3
+    q, k, v = qkv_bits(B, S, H, seed=17)
+    full = oracle.attention(q, k, v, 0.1)
+    for b in range(B):
+        for h in range(H):
+            sl = [np.ascontiguousarray(t[b:b + 1, :, h:h + 1]) for t in (q, k, v)]
+            one = oracle.attention(*sl, 0.1)
+            assert np.array_equal(one[0, :, 0], full[b, :, h])
+
+
+def test_row_subset_matches_full():
+    B, S, H = 2, 160, 2
+    q, k, v = qkv_bits(B, S, H, seed=18)
+    full = oracle.attention(q, k, v, 0.09)
+    rows = np.array([[0, 0, 0], [1, 1, 159], [0, 1, 77], [1, 0, 128]], np.int32)
+    sub = oracle.attention(q, k, v, 0.09, rows=rows)
+    for n, (b, h, i) in enumerate(rows):
+        assert np.array_equal(sub[n], full[b, i, h])
+
+
+def test_softmax_reading_max_column_is_448_and_fp32_sum():
+    q, k, v = qkv_bits(1, 300, 1, seed=19, recipe="k_channel_offset")
+    quant = oracle.quantize(q, k, v)
+    scale = 1 / math.sqrt(128)
+    s = oracle.qk_int32(quant[0], quant[2], 300)[0, 0].astype(np.float64)
+    for i in (0, 150, 299):
+        _, pc, L = oracle.attend_row_debug(quant, 300, scale, 0, 0, i)
+        dec = oracle.e4m3_decode(pc)
+        j = int(np.argmax(s[i] * quant[3][0, 0, np.arange(300) // 32]))
+        assert pc[j] == 0x7E
+        assert L == dec.sum() and dec.max() == 448.0
+        _, _, Lp = oracle.attend_row_debug(quant, 300, scale, 0, 0, i, l_mode=1)
+        assert abs(Lp - L) <= L * 2.0 ** -4         # e4m3 half-ulp relative bound
+
+
+# ------------------------------------------------------------- accuracy --
+
+def test_tiny_workload_cosine_vs_fp64():
+    w = WORKLOADS["b1_s256_h2"]
+    q, k, v = [bf16_bits(t) for t in make_workload(w)]
+    out = f32(oracle.attention(q, k, v, w.softmax_scale))
+    ref = oracle.attention_fp64(q, k, v, w.softmax_scale)
+    bar = math.floor(golden("cosine_vs_sdpa_head_dim_128") * 1000) / 1000   # 0.999
+    assert cosine(out, ref) >= bar
+
+
+# --------------------------------------------------- float64 reference --
+
+def test_fp64_reference_matches_torch_sdpa_float64():
+    q, k, v = qkv_bits(2, 70, 3, seed=20)
+    ref = oracle.attention_fp64(q, k, v, 0.07)
+    t = [torch.from_numpy(oracle.fp64_reference.bf16_bits_to_f64(x)).permute(0, 2, 1, 3)
+         for x in (q, k, v)]
+    sdpa = torch.nn.functional.scaled_dot_product_attention(*t, scale=0.07)
+    assert np.allclose(ref, sdpa.permute(0, 2, 1, 3).numpy(), rtol=0, atol=1e-12)
+    rows = np.array([[1, 2, 69], [0, 0, 3]], np.int32)
+    sub = oracle.attention_fp64(q, k, v, 0.07, rows=rows)
+    assert np.allclose(sub[0], ref[1, 69, 2], rtol=0, atol=1e-13)
+    assert np.allclose(sub[1], ref[0, 3, 0], rtol=0, atol=1e-13)
+
+
+def test_fp64_reference_zero_query_is_mean_of_v():
+    q = np.zeros((1, 50, 1, 128), np.uint16)
+    _, k, v = qkv_bits(1, 50, 1, seed=21)
+    ref = oracle.attention_fp64(q, k, v, 0.1)
+    mean = oracle.fp64_reference.bf16_bits_to_f64(v)[0, :, 0].mean(axis=0)
+    assert np.allclose(ref[0, :, 0], mean[None, :], rtol=0, atol=1e-14)
