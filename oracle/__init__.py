@@ -70,10 +70,10 @@ def _load():
         lib.oracle_qk_int32.argtypes = [P, P, I, I, I, I, I, P]
         lib.oracle_attend_rows.restype = I
         lib.oracle_attend_rows.argtypes = [P, P, P, P, P, P, I, I, I, I, I,
-                                           ctypes.c_float, I, P, ctypes.c_int64, P]
+                                           ctypes.c_float, I, P, ctypes.c_int64, P, P]
         lib.oracle_attend_row_debug.restype = I
         lib.oracle_attend_row_debug.argtypes = [P, P, P, P, P, P, I, I, I, I, I,
-                                                ctypes.c_float, I, I, I, I, P, P, P]
+                                                ctypes.c_float, I, I, I, I, P, P, P, P]
         lib.oracle_num_threads.restype = I
         _lib = lib
         return lib
@@ -155,23 +155,28 @@ def all_rows(B: int, S: int, H: int) -> np.ndarray:
     return np.stack([b.ravel(), h.ravel(), s.ravel()], axis=1).astype(np.int32)
 
 
-def attend_rows(quant, S: int, softmax_scale: float, rows: np.ndarray, l_mode: int = 0):
+def attend_rows(quant, S: int, softmax_scale: float, rows: np.ndarray, l_mode: int = 0,
+                return_ties: bool = False):
     """Attention output for selected query rows from quantised operands.
 
     quant = (q_codes, q_scale, k_codes, k_scale, vt_codes, v_scale) in the
     layouts returned by ``quantize_qk`` / ``quantize_v``.  rows: int32 [n, 3]
-    of (b, h, i).  Returns bf16 bits [n, D].
+    of (b, h, i).  Returns bf16 bits [n, D]; with return_ties also each row's
+    tie bound (float64 [n]): the most an equally correct rounding of P codes
+    that sit on an E4M3 rounding midpoint could move that row's outputs.
     """
     qc, qs, kc, ks, vt, vs = [np.ascontiguousarray(a) for a in quant]
     B, H, Sp, D = qc.shape
     rows = np.ascontiguousarray(rows, dtype=np.int32).reshape(-1, 3)
     out = np.empty((rows.shape[0], D), dtype=np.uint16)
+    ties = np.zeros(rows.shape[0], dtype=np.float64)
     rc = _load().oracle_attend_rows(_ptr(qc), _ptr(qs), _ptr(kc), _ptr(ks), _ptr(vt),
                                     _ptr(vs), B, S, H, D, Sp, float(softmax_scale),
-                                    int(l_mode), _ptr(rows), rows.shape[0], _ptr(out))
+                                    int(l_mode), _ptr(rows), rows.shape[0], _ptr(out),
+                                    _ptr(ties))
     if rc != 0:
         raise MemoryError("oracle_attend_rows failed to allocate")
-    return out
+    return (out, ties) if return_ties else out
 
 
 def attend_row_debug(quant, S: int, softmax_scale: float, b: int, h: int, i: int,
@@ -182,10 +187,11 @@ def attend_row_debug(quant, S: int, softmax_scale: float, b: int, h: int, i: int
     out = np.empty(D, dtype=np.uint16)
     pc = np.empty(S, dtype=np.uint8)
     L = ctypes.c_double(0.0)
+    tie = ctypes.c_double(0.0)
     rc = _load().oracle_attend_row_debug(_ptr(qc), _ptr(qs), _ptr(kc), _ptr(ks), _ptr(vt),
                                          _ptr(vs), B, S, H, D, Sp, float(softmax_scale),
                                          int(l_mode), b, h, i, _ptr(out), _ptr(pc),
-                                         ctypes.byref(L))
+                                         ctypes.byref(L), ctypes.byref(tie))
     if rc != 0:
         raise MemoryError("oracle_attend_row_debug failed to allocate")
     return out, pc, L.value
@@ -200,15 +206,17 @@ def quantize(q: np.ndarray, k: np.ndarray, v: np.ndarray):
 
 
 def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, softmax_scale: float,
-              rows: np.ndarray | None = None, l_mode: int = 0):
+              rows: np.ndarray | None = None, l_mode: int = 0, return_ties: bool = False):
     """Whole quantize-then-attend path from bf16 bits.
 
-    rows None: full output bf16 bits [B,S,H,D]; otherwise bf16 bits [n, D]
-    for the given (b, h, i) rows.
+    rows None: full output bf16 bits [B,S,H,D] (ties [B,S,H]); otherwise
+    bf16 bits [n, D] (ties [n]) for the given (b, h, i) rows.
     """
     B, S, H, D = q.shape
     quant = quantize(q, k, v)
     if rows is None:
-        out = attend_rows(quant, S, softmax_scale, all_rows(B, S, H), l_mode)
-        return out.reshape(B, S, H, D)
-    return attend_rows(quant, S, softmax_scale, rows, l_mode)
+        out, ties = attend_rows(quant, S, softmax_scale, all_rows(B, S, H), l_mode, True)
+        out, ties = out.reshape(B, S, H, D), ties.reshape(B, S, H)
+    else:
+        out, ties = attend_rows(quant, S, softmax_scale, rows, l_mode, True)
+    return (out, ties) if return_ties else out

@@ -29,17 +29,35 @@
  *      sv = amax / 448, code = e4m3(v / sv); an all-zero channel has sv = 0.
  *  R5  QK^T: integer products summed exactly.  |acc| <= 128 * 127^2 < 2^24,
  *      so FP32 accumulation of these products is exact too and equals INT32.
- *  R6  score s = ((float)acc * (sq * sk)) * softmax_scale, fp32, left to right.
- *  R7  softmax in FP32, two-pass: m = max_j s_j, p_j = fp32(exp(s_j - m))
- *      with s_j - m an fp32 subtraction and exp evaluated in double then
- *      rounded once to fp32.
- *  R8  P to FP8: code_j = e4m3(p_j * 448) (fp32 product).
- *  R9  normaliser L = sum_j dec(code_j) (the applied quantised weights);
- *      l_mode = 1 selects the alternative L = sum_j 448 * p_j.
- *  R10 PV: O[d] = sum_j dec(pcode_j) * dec(vcode_jd).  Every product is a
- *      multiple of 2^-18 below 2^18 and there are at most 2^16 terms, so the
- *      double sum is exact and order-independent.
+ *  R6  scores in the base-2 domain, fp32, in this order:
+ *      c = fl(softmax_scale * L2E) (L2E = the fp32 value nearest log2 e),
+ *      c_row = fl(sq * c), cb_j = fl(c_row * sk_{j/32}), x_j = fl(acc_j * cb_j),
+ *      so that exp(s_j - s_k) = 2^(x_j - x_k) with s = acc * sq * sk *
+ *      softmax_scale.  The kernel takes the FP8 decisions of R8 from these
+ *      same fp32 values, so both sides decide every P code in one precision.
+ *  R7  online softmax in FP32 over KV tiles of 128 keys (keys [128t,
+ *      128t+128) that exist): the running max m_t = max(m_{t-1}, max_{j in
+ *      t} x_j) (m_{-1} = -inf); bias_t = fl(m_t - LOG2_448) with LOG2_448 =
+ *      fp32(log2 448); p_j = fp32(2^fmaf(acc_j, cb_j, -bias_t)) (2^ in double,
+ *      rounded once), so p_j <= 448 is 448 * exp(s_j - running max);
+ *      alpha_t = fp32(2^fl(m_{t-1} - m_t)) rescales what was accumulated
+ *      (alpha_0 = 0).
+ *  R8  P to FP8 per tile, against the running max: code_j = e4m3(p_j).
+ *  R9  normaliser L = alpha_t * L + sum_{j in t} dec(code_j) (the applied
+ *      quantised weights, in double); l_mode = 1 selects the alternative
+ *      L = alpha_t * L + sum_{j in t} p_j (the unquantised FP32 weights).
+ *  R10 PV: O[d] = alpha_t * O[d] + sum_{j in t} dec(code_j) dec(vcode_jd) in
+ *      double.  Within a tile every product is a multiple of 2^-18 below
+ *      2^18, so each tile's sum is exact and independent of key order.
  *  R11 out[d] = bf16_rne((float)(O[d] * sv[d] / L)), layout [B, S, H, D].
+ *
+ *  Tie bound.  A P code whose p_j lies within 2^-19 (relative) of a
+ *  rounding midpoint of the E4M3 grid is a tie: an implementation whose 2^x
+ *  differs from the correctly rounded one by a few ulp may round it the other
+ *  way, and both results are correct.  For each row the oracle reports
+ *  bound = T * 2 * vmax / (L - T), with T the weight (in final units) such
+ *  ties could move and vmax = 448 * max_d sv[d]: the most any such flip can
+ *  change any output of the row.  Rows without ties have bound 0.
  *
  * Build: gcc -O2 -fopenmp -ffp-contract=off -fno-fast-math -shared -fPIC
  */
@@ -194,53 +212,96 @@ int oracle_qk_int32(const int8_t *q, const int8_t *k, int B, int S, int H,
 
 /* ------------------------------------------------------- attention -- */
 
+/* The fp32 value nearest log2(e), and fp32(log2(448)). */
+#define ORACLE_L2E 1.44269502162933349609375f
+#define ORACLE_LOG2_448 8.80735492706298828125f
+#define ORACLE_KV_TILE 128
+#define ORACLE_TIE_REL 1.9073486328125e-06 /* 2^-19 */
+
+/* Distance of an E4M3 code's value to the other side of the nearest rounding
+ * midpoint: if y (the fp32 value encoded) is within ORACLE_TIE_REL of a
+ * midpoint, returns |value of the neighbouring code - value of code|, else 0. */
+static double tie_step(float y, uint8_t code) {
+    double a = fabs((double)y);
+    if (a >= 448.0 || a == 0.0) return 0.0;
+    int e;
+    (void)frexp(a, &e);
+    e -= 1;
+    if (e < -6) e = -6;
+    double quantum = ldexp(1.0, e - 3);
+    double f = a / quantum;
+    double mid = floor(f) + 0.5;
+    if (fabs(f - mid) * quantum > ORACLE_TIE_REL * a) return 0.0;
+    double v = fabs(oracle_e4m3_decode(code));
+    double other = (v >= mid * quantum) ? floor(f) * quantum : (floor(f) + 1.0) * quantum;
+    if (other > 448.0) other = 448.0;
+    return fabs(other - v);
+}
+
 /* One query row (b, h, i).  Writes D bf16 outputs to out_row.  If pcodes is
- * not NULL it receives the S FP8 codes of P and *L_out the normaliser.
- * vdec is this head's decoded V, [S][D] floats (exact).  R6..R11. */
+ * not NULL it receives the S FP8 codes of P (each against the running max of
+ * its tile) and *L_out the normaliser; *tie_out (if not NULL) the row's tie
+ * bound.  vdec is this head's decoded V, [S][D] floats (exact); acc is
+ * scratch for one tile's integer scores.  R6..R11. */
 static void attend_row(const int8_t *q, const float *qs, const int8_t *k,
                        const float *ks, const float *vdec, const float *vs,
                        int b, int h, int i, int S, int H, int D, int S_pad,
                        float softmax_scale, int l_mode, float *sbuf,
-                       uint8_t *cbuf, double *obuf, uint16_t *out_row,
-                       uint8_t *pcodes, double *L_out) {
+                       int32_t *acc, uint8_t *cbuf, double *obuf, uint16_t *out_row,
+                       uint8_t *pcodes, double *L_out, double *tie_out) {
     int nb = (S + 31) / 32;
     const int8_t *qi = q + (((size_t)b * H + h) * S_pad + i) * D;
+    const float *vsh = vs + ((size_t)b * H + h) * D;
     float sq = qs[((size_t)b * H + h) * nb + i / 32];
-    /* scores (R5, R6) */
-    float m = -INFINITY;
-    for (int j = 0; j < S; ++j) {
-        const int8_t *kj = k + (((size_t)b * H + h) * S_pad + j) * D;
-        int32_t acc = 0;
-        for (int c = 0; c < D; ++c) acc += (int32_t)qi[c] * (int32_t)kj[c];
-        float sk = ks[((size_t)b * H + h) * nb + j / 32];
-        float s = ((float)acc * (sq * sk)) * softmax_scale;
-        sbuf[j] = s;
-        if (s > m) m = s;
-    }
-    /* probabilities, FP8 codes, normaliser (R7, R8, R9) */
-    double L = 0.0;
-    for (int j = 0; j < S; ++j) {
-        float t = sbuf[j] - m;
-        float p = (float)exp((double)t);
-        uint8_t c = oracle_e4m3_encode(p * 448.0f);
-        cbuf[j] = c;
-        L += l_mode ? 448.0 * (double)p : oracle_e4m3_decode(c);
-    }
-    /* PV with exact products and exact double sums (R10) */
+    float c = softmax_scale * ORACLE_L2E;
+    float c_row = sq * c;
+    double L = 0.0, T = 0.0;
+    float m_run = -INFINITY;
     for (int d = 0; d < D; ++d) obuf[d] = 0.0;
-    for (int j = 0; j < S; ++j) {
-        double w = oracle_e4m3_decode(cbuf[j]);
-        if (w == 0.0) continue;
-        const float *vj = vdec + (size_t)j * D;
-        for (int d = 0; d < D; ++d) obuf[d] += w * (double)vj[d];
+    for (int j0 = 0; j0 < S; j0 += ORACLE_KV_TILE) {
+        int j1 = j0 + ORACLE_KV_TILE < S ? j0 + ORACLE_KV_TILE : S;
+        /* integer scores (R5) and their base-2 values (R6); sbuf keeps cb_j */
+        float m_tile = -INFINITY;
+        for (int j = j0; j < j1; ++j) {
+            const int8_t *kj = k + (((size_t)b * H + h) * S_pad + j) * D;
+            int32_t a = 0;
+            for (int cc = 0; cc < D; ++cc) a += (int32_t)qi[cc] * (int32_t)kj[cc];
+            float cb = c_row * ks[((size_t)b * H + h) * nb + j / 32];
+            float x = (float)a * cb;
+            acc[j - j0] = a;
+            sbuf[j] = cb;
+            if (x > m_tile) m_tile = x;
+        }
+        /* running max, rescale of what was accumulated (R7, R9, R10) */
+        float m_new = m_run > m_tile ? m_run : m_tile;
+        double alpha = (m_run == -INFINITY) ? 0.0 : (double)(float)exp2((double)(m_run - m_new));
+        float bias = m_new - ORACLE_LOG2_448;
+        L *= alpha;
+        T *= alpha;
+        for (int d = 0; d < D; ++d) obuf[d] *= alpha;
+        for (int j = j0; j < j1; ++j) {
+            float p = (float)exp2((double)fmaf((float)acc[j - j0], sbuf[j], -bias));
+            uint8_t code = oracle_e4m3_encode(p);           /* R8 */
+            double w = oracle_e4m3_decode(code);
+            cbuf[j] = code;
+            L += l_mode ? (double)p : w;
+            T += tie_step(p, code);
+            if (w == 0.0) continue;
+            const float *vj = vdec + (size_t)j * D;
+            for (int d = 0; d < D; ++d) obuf[d] += w * (double)vj[d];
+        }
+        m_run = m_new;
     }
     /* epilogue (R11) */
+    double vmax = 0.0;
     for (int d = 0; d < D; ++d) {
-        double o = obuf[d] * (double)vs[((size_t)b * H + h) * D + d] / L;
+        double o = obuf[d] * (double)vsh[d] / L;
         out_row[d] = f32_to_bf16_rne((float)o);
+        if (448.0 * (double)vsh[d] > vmax) vmax = 448.0 * (double)vsh[d];
     }
     if (pcodes) memcpy(pcodes, cbuf, (size_t)S);
     if (L_out) *L_out = L;
+    if (tie_out) *tie_out = (T > 0.0 && L > T) ? T * 2.0 * vmax / (L - T) : (T > 0.0 ? INFINITY : 0.0);
 }
 
 /* Decode one head's V^T codes into [S][D] floats (e4m3 values are exact in
@@ -255,14 +316,15 @@ static void decode_v_head(const uint8_t *vt, int b, int h, int S, int H, int D,
 
 /* Attention output for a list of query rows.  rows: n triples (b, h, i).
  * out: bf16 [n, D] in the order of rows.  Every (b, h) named in rows must
- * appear; heads are decoded once.  Returns 0, or -1 on allocation failure.
+ * appear; heads are decoded once.  ties (may be NULL): double [n], each
+ * row's tie bound.  Returns 0, or -1 on allocation failure.
  * [I15014] bullets 1-2, [P15060] ("no LSE"): the output is the normalised
  * attention only. */
 int oracle_attend_rows(const int8_t *q, const float *qs, const int8_t *k,
                        const float *ks, const uint8_t *vt, const float *vs,
                        int B, int S, int H, int D, int S_pad,
                        float softmax_scale, int l_mode, const int32_t *rows,
-                       int64_t n, uint16_t *out) {
+                       int64_t n, uint16_t *out, double *ties) {
     /* decode the heads in use */
     int nheads = B * H;
     float **vdec = (float **)calloc((size_t)nheads, sizeof(float *));
@@ -282,9 +344,10 @@ int oracle_attend_rows(const int8_t *q, const float *qs, const int8_t *k,
 #pragma omp parallel
         {
             float *sbuf = (float *)malloc((size_t)S * sizeof(float));
+            int32_t *abuf = (int32_t *)malloc(ORACLE_KV_TILE * sizeof(int32_t));
             uint8_t *cbuf = (uint8_t *)malloc((size_t)S);
             double *obuf = (double *)malloc((size_t)D * sizeof(double));
-            if (!sbuf || !cbuf || !obuf) {
+            if (!sbuf || !abuf || !cbuf || !obuf) {
 #pragma omp atomic write
                 fail = 1;
             } else {
@@ -292,11 +355,11 @@ int oracle_attend_rows(const int8_t *q, const float *qs, const int8_t *k,
                 for (int64_t r = 0; r < n; ++r) {
                     int b = rows[3 * r], h = rows[3 * r + 1], i = rows[3 * r + 2];
                     attend_row(q, qs, k, ks, vdec[b * H + h], vs, b, h, i, S, H, D,
-                               S_pad, softmax_scale, l_mode, sbuf, cbuf, obuf,
-                               out + (size_t)r * D, NULL, NULL);
+                               S_pad, softmax_scale, l_mode, sbuf, abuf, cbuf, obuf,
+                               out + (size_t)r * D, NULL, NULL, ties ? ties + r : NULL);
                 }
             }
-            free(sbuf); free(cbuf); free(obuf);
+            free(sbuf); free(abuf); free(cbuf); free(obuf);
         }
     }
     for (int bh = 0; bh < nheads; ++bh) free(vdec[bh]);
@@ -310,20 +373,22 @@ int oracle_attend_row_debug(const int8_t *q, const float *qs, const int8_t *k,
                             const float *ks, const uint8_t *vt, const float *vs,
                             int B, int S, int H, int D, int S_pad,
                             float softmax_scale, int l_mode, int b, int h, int i,
-                            uint16_t *out_row, uint8_t *pcodes, double *L_out) {
+                            uint16_t *out_row, uint8_t *pcodes, double *L_out,
+                            double *tie_out) {
     (void)B;
     float *vdec = (float *)malloc((size_t)S * D * sizeof(float));
     float *sbuf = (float *)malloc((size_t)S * sizeof(float));
+    int32_t *abuf = (int32_t *)malloc(ORACLE_KV_TILE * sizeof(int32_t));
     uint8_t *cbuf = (uint8_t *)malloc((size_t)S);
     double *obuf = (double *)malloc((size_t)D * sizeof(double));
     int rc = -1;
-    if (vdec && sbuf && cbuf && obuf) {
+    if (vdec && sbuf && abuf && cbuf && obuf) {
         decode_v_head(vt, b, h, S, H, D, S_pad, vdec);
         attend_row(q, qs, k, ks, vdec, vs, b, h, i, S, H, D, S_pad, softmax_scale,
-                   l_mode, sbuf, cbuf, obuf, out_row, pcodes, L_out);
+                   l_mode, sbuf, abuf, cbuf, obuf, out_row, pcodes, L_out, tie_out);
         rc = 0;
     }
-    free(vdec); free(sbuf); free(cbuf); free(obuf);
+    free(vdec); free(sbuf); free(abuf); free(cbuf); free(obuf);
     return rc;
 }
 
