@@ -1,0 +1,393 @@
+#!/usr/bin/env python3
+"""Benchmark of the quantized attention forward on GB300.
+
+One step = one pass of the whole hot path over one batch: quantise Q/K/V
+(INT8 per 32-token block, E4M3 per V channel) and run the fused attention
+kernel, through the C ABI (``sage_attn_fwd``).  The metric is the pages'
+attention throughput, TOPS = 4*B*H*S^2*D / step time.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                  [--impl ours|reference]
+
+N > 1 runs N independent replicas (one process per GPU under torchrun; the
+method has no exchange step on one call), reports the whole-job throughput
+and takes the maximum time over ranks.  ``--impl reference`` times the CPU
+oracle (the only stand-in for a reference implementation: none exists for
+this hardware) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "quantized attention TOPS (4*B*H*S^2*D/s)"
+UNIT = "TOPS"
+DTYPE = "int8+e4m3"          # INT8 QK^T (exact, FP32 accumulate), E4M3 PV (FP32 accumulate)
+DEFAULT_WORKLOAD = "b2_s16384_h24_outlier"
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "attention_traffic.json")
+ATTN_SOURCES = [os.path.join(ROOT, "quantized_attention_diffusion_gb300", "csrc", f)
+                for f in ("attention.cu", "sm103_ptx.cuh")]
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="approximate CPU time budget of the oracle baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------ processes --
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+class Group:
+    """Barrier and max-reduce across ranks (no data-path collective)."""
+
+    def __init__(self, world, rank, local, use_cuda):
+        self.world, self.rank = world, rank
+        self.dist = None
+        if world > 1:
+            import torch.distributed as dist
+            os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+            dist.init_process_group("nccl" if use_cuda else "gloo")
+            self.dist = dist
+
+    def barrier(self):
+        if self.dist:
+            self.dist.barrier()
+
+    def max(self, x: float) -> float:
+        if not self.dist:
+            return x
+        import torch
+        dev = torch.device("cuda", torch.cuda.current_device()) if torch.cuda.is_available() else "cpu"
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        self.dist.all_reduce(t, op=self.dist.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.dist:
+            self.dist.destroy_process_group()
+
+
+# --------------------------------------------------------------- clocks --
+
+class ClockSampler:
+    """nvidia-smi samples (every 200 ms) of the SM clock and throttle reasons."""
+
+    FIELDS = ["clocks.sm", "clocks.max.sm", "clocks_event_reasons.hw_slowdown",
+              "clocks_event_reasons.hw_thermal_slowdown", "clocks_event_reasons.sw_thermal_slowdown",
+              "clocks_event_reasons.sw_power_cap", "power.draw"]
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.TemporaryFile(mode="w+")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={','.join(self.FIELDS)}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.seek(0)
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.file.read().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) != len(self.FIELDS):
+                continue
+            try:
+                sm.append(float(f[0]))
+                smax.append(float(f[1]))
+                power.append(float(f[6]))
+            except ValueError:
+                continue
+            for n, val in zip(names, f[2:6]):
+                if val.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm), "power_w_max": max(power) if power else None}
+
+
+# ---------------------------------------------------------------- peaks --
+
+def tensor_peak():
+    """Dense peak of the attention kernel's mixed contraction (TFLOP/s).
+
+    QK^T runs at the fp16/bf16 tensor rate (the measured cuBLAS bf16 figure),
+    PV at the E4M3 rate (2x, the nominal fp8/bf16 ratio).  Half the ops run
+    at each rate, so the combined peak is 4 / (2/P + 2/(2P)) = 4P/3.  The
+    sustained figure applies: the kernel runs back to back for the whole
+    timed region.
+    """
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    src = "fallback"
+    p_bf16, hbm = 1700.0, 6800.0
+    try:
+        with open(path) as f:
+            m = json.load(f)
+        p_bf16 = float(m["bf16_tflops_sustained"])
+        hbm = float(m["hbm_gbs"])
+        src = "measured"
+    except (OSError, KeyError, ValueError):
+        pass
+    return 4.0 * p_bf16 / 3.0, p_bf16, hbm, src
+
+
+def attention_traffic():
+    """dram bytes per attention launch from the committed ncu summary, or
+    None if the kernel source changed since it was captured."""
+    try:
+        with open(PROFILE_TRAFFIC) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    h = hashlib.sha256()
+    for p in ATTN_SOURCES:
+        with open(p, "rb") as f:
+            h.update(f.read())
+    if rec.get("source_sha256") != h.hexdigest():
+        return None
+    return rec.get("dram_bytes_per_launch_full")
+
+
+# -------------------------------------------------------- oracle timing --
+
+def oracle_sample(w, q, k, v, seconds: float, steps: int = 1):
+    """Time the CPU oracle on a bounded sample: one (batch, head) of the
+    workload, quantised whole, and as many of its query rows as fit in
+    `seconds` per step.  Returns (TOPS, sample text, cores, s_per_step)."""
+    import numpy as np
+
+    import oracle
+    from quantized_attention_diffusion_gb300.workloads import bf16_bits
+
+    b, h = 0, 0
+    sl = [np.ascontiguousarray(bf16_bits(t[b:b + 1, :, h:h + 1, :])) for t in (q, k, v)]
+
+    def run(n_rows):
+        t0 = time.perf_counter()
+        quant = oracle.quantize(*sl)
+        rows = np.stack([np.zeros(n_rows), np.zeros(n_rows),
+                         np.linspace(0, w.S - 1, n_rows).round()], axis=1).astype(np.int32)
+        oracle.attend_rows(quant, w.S, w.softmax_scale, rows)
+        return time.perf_counter() - t0
+
+    n_cal = 64
+    t_cal = run(n_cal)
+    t_quant = max(1e-3, run(1))
+    per_row = max(1e-7, (t_cal - t_quant) / (n_cal - 1))
+    n_rows = int(max(8, min(w.S, (seconds - t_quant) / per_row)))
+    times = [run(n_rows) for _ in range(steps)]
+    t = statistics.median(times) if steps > 1 else times[0]
+    ops = 4.0 * n_rows * w.S * w.D
+    sample = (f"one (b,h) of {w.name}: quantise its {w.S} tokens, then attention for {n_rows} "
+              f"of its query rows ({ops:.3g} ops)")
+    return ops / t / 1e12, sample, oracle.num_threads(), ops, times
+
+
+# ------------------------------------------------------------------ ours --
+
+def run_ours(args, group, local):
+    import torch
+
+    import quantized_attention_diffusion_gb300 as qad
+    from quantized_attention_diffusion_gb300.workloads import WORKLOADS, make_workload
+
+    w = WORKLOADS[args.workload]
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    qad.load_library()
+    q_h, k_h, v_h = make_workload(w)                       # CPU, seeded
+    q, k, v = (t.to(dev) for t in (q_h, k_h, v_h))
+    out = torch.empty_like(q)
+    K, W = args.steps, args.warmup
+
+    for _ in range(W):
+        qad.attn_fwd(q, k, v, w.softmax_scale, out=out)
+    torch.cuda.synchronize()
+
+    # per-step events around the attention kernel (materialise handles first)
+    before = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    after = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    for e in before + after:
+        e.record()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    sampler = ClockSampler(local)
+    group.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.3)
+    start.record()
+    for i in range(K):
+        qad.set_attention_events(before[i], after[i])
+        qad.attn_fwd(q, k, v, w.softmax_scale, out=out)
+    end.record()
+    torch.cuda.synchronize()
+    qad.set_attention_events()
+    group.barrier()
+    clocks = sampler.stop()
+    ms = start.elapsed_time(end)
+    attn_ms = statistics.mean(b.elapsed_time(a) for b, a in zip(before, after))
+    ms_max = group.max(ms)
+    attn_ms_max = group.max(attn_ms)
+    value = group.world * w.ops * K / (ms_max * 1e-3) / 1e12
+
+    # end to end through the public API with host buffers: pinned H2D of
+    # Q/K/V, the call, D2H of the output, every step inside the timed region
+    K2 = max(3, min(K, 20))
+    qp, kp, vp = (t.pin_memory() for t in (q_h, k_h, v_h))
+    outp = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    qd, kd, vd = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+
+    def e2e_step():
+        qd.copy_(qp, non_blocking=True)
+        kd.copy_(kp, non_blocking=True)
+        vd.copy_(vp, non_blocking=True)
+        qad.attn_fwd(qd, kd, vd, w.softmax_scale, out=out)
+        outp.copy_(out, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    group.barrier()
+    s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s2.record()
+    for _ in range(K2):
+        e2e_step()
+    e2.record()
+    torch.cuda.synchronize()
+    group.barrier()
+    e2e_ms = group.max(s2.elapsed_time(e2))
+    e2e_value = group.world * w.ops * K2 / (e2e_ms * 1e-3) / 1e12
+    in_bytes = 3 * q.numel() * q.element_size()
+    out_bytes = out.numel() * out.element_size()
+
+    peak, p_bf16, hbm, src = tensor_peak()
+    achieved = w.ops / (attn_ms_max * 1e-3) / 1e12
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": UNIT,
+        "n_gpus": group.world,
+        "steps": K,
+        "warmup": W,
+        "ms_per_step": round(ms_max / K, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": DTYPE,
+        "data": "synthetic (seeded; shapes and distributions of the pages' diffusion workloads)",
+        "config": {
+            "workload": w.name, "B": w.B, "S": w.S, "H": w.H, "D": w.D, "recipe": w.recipe,
+            "seed": w.seed, "softmax_scale": w.softmax_scale, "path": "sage_attn_fwd (quantise + attention)",
+            "l2": f"inputs larger than L2 ({in_bytes / 1e6:.0f} MB read per step, L2 129 MB)",
+            "parallelism": "replicas" if group.world > 1 else "single GPU",
+        },
+        "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": in_bytes,
+                "d2h_bytes_per_step": out_bytes, "steps": K2},
+        "gpu_launches": 4 * K,
+        "roofline": {
+            "bound": "tensor", "achieved": round(achieved, 1), "peak": round(peak, 1), "unit": "TFLOP/s",
+            "frac": round(achieved / peak, 4), "traffic": attention_traffic(),
+            "kernel": "sage_attn_kernel", "attention_ms_per_launch": round(attn_ms_max, 4),
+            "peak_basis": f"{src} bf16 sustained {p_bf16} TFLOP/s for QK^T (fp16 rate), x2 for E4M3 PV",
+        },
+        "clocks": clocks,
+    }
+    if group.rank == 0 and group.world == 1 and not args.no_cpu_baseline:
+        tops, sample, cores, _, _ = oracle_sample(w, q_h, k_h, v_h, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": round(tops, 6), "unit": UNIT, "cores": cores,
+                                "kind": "oracle", "sample": sample}
+    return line
+
+
+# ------------------------------------------------------------- reference --
+
+def run_reference(args):
+    from quantized_attention_diffusion_gb300.workloads import WORKLOADS, make_workload
+
+    w = WORKLOADS[args.workload]
+    q, k, v = make_workload(w)
+    K, W = args.steps, args.warmup
+    per_step = max(0.05, min(2.0, 150.0 / max(1, K + W)))
+    _, sample, cores, ops, times = oracle_sample(w, q, k, v, per_step, steps=K + W)
+    timed = times[W:] if len(times) > W else times
+    t = statistics.mean(timed)
+    value = ops / t / 1e12
+    return {
+        "impl": "reference",
+        "metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": 1, "steps": K, "warmup": W,
+        "ms_per_step": round(t * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": DTYPE,
+        "data": "synthetic (seeded; shapes and distributions of the pages' diffusion workloads)",
+        "config": {"workload": w.name, "B": w.B, "S": w.S, "H": w.H, "D": w.D, "recipe": w.recipe,
+                   "seed": w.seed, "softmax_scale": w.softmax_scale,
+                   "path": "CPU oracle (plain C, OpenMP) on a bounded sample per step"},
+        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse_args()
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+    import torch
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (the attention path has no CPU fallback)")
+    group = Group(world, rank, local, use_cuda=True)
+    try:
+        line = run_ours(args, group, local)
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+    finally:
+        group.close()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,175 @@
+/*
+ * sage.h -- C ABI of the GB300 (sm_103a) SageAttention-style quantized
+ * attention forward.
+ *
+ * The method (diffusers issue #15014 "gfx1201 (RDNA4) SageAttention attention
+ * backend: aiter package or Hub kernel?", section "Is your feature request
+ * related to a problem?", kernel contract bullets):
+ *   - INT8 QK^T and FP8 PV with FP32 accumulation;
+ *   - Q and K quantized per 32-row block, V per channel;
+ *   - inputs BF16 [B, S, H, 128], Q/K/V of equal shape, no mask, non-causal.
+ * diffusers PR #15060 "Add aiter_sage_hub attention backend for AMD RDNA4
+ * (gfx1201)", "What does this PR do?": head dim 128 only; inference only; the
+ * kernel returns no LSE.  The same issue, "Describe the solution you'd
+ * like": unsupported inputs are rejected with a clear error.
+ *
+ * Conventions for every entry point:
+ *   - Pointers are device pointers unless stated otherwise; the caller owns
+ *     every buffer.  Tensors are dense and row-major in the layouts given.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Calls are stream-ordered and asynchronous; none synchronises
+ *     the host except sage_sync_status().
+ *   - All argument checks run on the host before any launch; a failed check
+ *     launches nothing.  On failure the call returns a non-zero sage_status
+ *     and sage_last_error() describes it (thread-local text).
+ *   - Nothing traps on the device.  A device-side wait that runs past its
+ *     limit records SAGE_ERR_TIMEOUT in a per-device error word, which
+ *     sage_sync_status() reports.
+ *   - Shapes: B, S, H >= 1; D must be 128.  B*H <= 2^31-1.
+ *     S_pad = ceil(S / 128) * 128, nb = ceil(S / 32).
+ */
+#ifndef SAGE_H_
+#define SAGE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum sage_status {
+  SAGE_OK = 0,
+  SAGE_ERR_INVALID_ARG = 1, /* a size < 1, a NULL pointer, a non-finite or non-positive scale */
+  SAGE_ERR_UNSUPPORTED = 2, /* head dimension other than 128 */
+  SAGE_ERR_MISALIGNED = 3,  /* a pointer not 16-byte aligned */
+  SAGE_ERR_CUDA = 4,        /* a CUDA runtime or launch error (message kept) */
+  SAGE_ERR_NO_MEMORY = 5,   /* workspace allocation failed */
+  SAGE_ERR_TIMEOUT = 6,     /* a device wait gave up (reported by sage_sync_status) */
+  SAGE_ERR_WORKSPACE = 7    /* caller workspace smaller than sage_workspace_bytes() */
+} sage_status;
+
+/* Head dimension, Q/K quantisation block and tile sizes of this library. */
+#define SAGE_HEAD_DIM 128
+#define SAGE_QK_BLOCK 32
+#define SAGE_TILE 128
+
+/* S rounded up to a multiple of 128 (the token extent of the quantised
+ * layouts).  Returns 0 for S < 1. */
+int64_t sage_padded_len(int S);
+
+/* Bytes of device workspace sage_attn_fwd_ws() / sage_attn_fwd_quantized()
+ * need for this shape (0 if the shape is invalid).  Layout is private. */
+size_t sage_workspace_bytes(int B, int S, int H, int D);
+
+/*
+ * sage_quantize_qkv -- quantise BF16 Q, K, V.
+ * Passage: the issue's contract bullet "Q/K are quantized per 32-row block
+ * and V per channel"; "FP8 PV" (PR #15060, "What does this PR do?").
+ *
+ *   q, k, v   in : bf16 [B, S, H, D]
+ *   q_i8      out: int8 [B, H, S_pad, D]; rows >= S are 0
+ *   q_scale   out: fp32 [B, H, nb]; block j covers tokens [32j, 32j+32) of
+ *                  one (batch, head): scale = amax / 127,
+ *                  code = clamp(rint(x / scale), -127, 127) (fp32 RNE
+ *                  divisions); an all-zero block has scale 0 and codes 0
+ *   k_i8, k_scale out: same for K
+ *   vt_fp8    out: E4M3FN codes of V transposed, [B, H, D, S_pad];
+ *                  columns >= S are 0
+ *   v_scale   out: fp32 [B, H, D]: sv = amax over all S tokens of the
+ *                  channel / 448, code = e4m3_rn_satfinite(v / sv)
+ * Errors: INVALID_ARG, UNSUPPORTED, MISALIGNED (every pointer 16-byte
+ * aligned), CUDA.  Uses 4*B*H*D bytes of scratch allocated from a private
+ * stream-ordered pool (NO_MEMORY if that fails).
+ */
+sage_status sage_quantize_qkv(const void* q, const void* k, const void* v, int B, int S, int H, int D,
+                              int8_t* q_i8, float* q_scale, int8_t* k_i8, float* k_scale,
+                              uint8_t* vt_fp8, float* v_scale, void* stream);
+
+/*
+ * sage_attn_fwd -- the whole path: quantise Q/K/V, then fused quantized
+ * attention.  Passage: the issue's contract bullets (INT8 QK^T, FP8 PV,
+ * FP32 accumulation; BF16 [B, S, H, 128]; no mask, non-causal) and
+ * aiter.gfx1201_sage_attention(q, k, v, softmax_scale) as named there.
+ *
+ *   q, k, v        in : bf16 [B, S, H, D]
+ *   out            out: bf16 [B, S, H, D] = softmax(QK^T * softmax_scale) V
+ *                       computed by the quantised algorithm; no LSE
+ *   softmax_scale  in : finite, > 0 (typically 1/sqrt(D))
+ * The workspace (sage_workspace_bytes) is taken from a private
+ * stream-ordered memory pool on `stream` and released in stream order, so
+ * concurrent calls on different streams do not share it.
+ * Errors: INVALID_ARG, UNSUPPORTED, MISALIGNED, NO_MEMORY, CUDA.
+ */
+sage_status sage_attn_fwd(const void* q, const void* k, const void* v, void* out, int B, int S, int H,
+                          int D, float softmax_scale, void* stream);
+
+/* As sage_attn_fwd, with caller-owned workspace of at least
+ * sage_workspace_bytes(B, S, H, D) bytes (256-byte aligned).  Calls that
+ * share a workspace must not overlap on the GPU.  Extra error: WORKSPACE. */
+sage_status sage_attn_fwd_ws(const void* q, const void* k, const void* v, void* out, int B, int S,
+                             int H, int D, float softmax_scale, void* workspace,
+                             size_t workspace_bytes, void* stream);
+
+/*
+ * sage_attn_fwd_quantized -- the attention step alone, from operands in the
+ * layouts sage_quantize_qkv() writes (same passage as sage_attn_fwd).
+ * `workspace` (caller-owned, >= sage_workspace_bytes) receives fp16 copies of
+ * the INT8 codes that feed the tensor cores.  Extra error: WORKSPACE.
+ */
+sage_status sage_attn_fwd_quantized(const int8_t* q_i8, const float* q_scale, const int8_t* k_i8,
+                                    const float* k_scale, const uint8_t* vt_fp8,
+                                    const float* v_scale, void* out, int B, int S, int H, int D,
+                                    float softmax_scale, void* workspace, size_t workspace_bytes,
+                                    void* stream);
+
+/*
+ * sage_debug_qk_int32 -- test entry: runs sage_attn_fwd_quantized and also
+ * writes the exact integer Q K^T accumulators the tensor cores produced,
+ * s_out int32 [B, H, S, S] (device, caller-owned; B*H*S*S*4 bytes).
+ * Passage: "INT8 QK^T ... with FP32 accumulation" (issue #15014); the
+ * accumulators are integers below 2^24 and equal the INT32 dot products.
+ */
+sage_status sage_debug_qk_int32(const int8_t* q_i8, const float* q_scale, const int8_t* k_i8,
+                                const float* k_scale, const uint8_t* vt_fp8, const float* v_scale,
+                                void* out, int32_t* s_out, int B, int S, int H, int D,
+                                float softmax_scale, void* workspace, size_t workspace_bytes,
+                                void* stream);
+
+/*
+ * sage_debug_wait_timeout -- test entry for failure detection without a GPU
+ * fault: launches one warp that waits on an mbarrier nothing arrives on,
+ * with a limit of timeout_ns (1..10^10).  The wait gives up, records
+ * SAGE_ERR_TIMEOUT in the device error word and the kernel returns;
+ * sage_sync_status() then reports it.  No counterpart on the pages.
+ */
+sage_status sage_debug_wait_timeout(uint64_t timeout_ns, void* stream);
+
+/* Synchronise `stream`, then report (and clear) the device error word of the
+ * current device: SAGE_OK, SAGE_ERR_TIMEOUT, or SAGE_ERR_CUDA if the stream
+ * itself failed. */
+sage_status sage_sync_status(void* stream);
+
+/* Limit, in nanoseconds, of every device-side wait in later launches from
+ * this process (default 2 s; 0 restores the default). */
+void sage_set_wait_timeout_ns(uint64_t ns);
+
+/* Timing hook (no counterpart on the pages): while set, every
+ * sage_attn_fwd / sage_attn_fwd_ws call made by this thread records `before`
+ * on its stream immediately before launching its attention kernel and
+ * `after` immediately after, so that the kernel's own duration can be read
+ * with cudaEventElapsedTime.  Both are cudaEvent_t passed as void*, owned by
+ * the caller; (NULL, NULL) clears the hook. */
+void sage_set_attention_events(void* before, void* after);
+
+/* Thread-local text of the last failure on this thread ("" if none). */
+const char* sage_last_error(void);
+
+/* Static name of a status code. */
+const char* sage_status_string(sage_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SAGE_H_ */

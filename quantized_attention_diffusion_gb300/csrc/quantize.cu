@@ -1,0 +1,259 @@
+// quantize.cu -- HBM-bound quantisation kernels (sm_103a).
+//
+// Q/K: INT8 per 32-token block of one (batch, head), one fp32 scale per block
+// (diffusers issue #15014 "gfx1201 (RDNA4) SageAttention attention backend",
+// kernel contract: "Q/K are quantized per 32-row block").  scale = amax/127,
+// code = clamp(rint(x/scale), -127, 127) with correctly rounded fp32
+// divisions, so the codes are bit-identical to a plain CPU statement.
+//
+// V: FP8 E4M3 per channel of one (batch, head) over all tokens (same passage:
+// "V per channel"; diffusers PR #15060 "Add aiter_sage_hub attention backend",
+// "What does this PR do?": FP8 PV).  sv = amax/448, code = e4m3_rn_sat(v/sv).
+// V is written transposed, [B, H, 128, S_pad], so that the attention kernel's
+// PV operand is K-major.
+//
+// This file is compiled without fast-math and without flush-to-zero: the
+// divisions are IEEE round-to-nearest-even (div.rn.f32).
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "sage_internal.cuh"
+#include "sm103_ptx.cuh"
+
+namespace sage {
+
+namespace {
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+__device__ __forceinline__ int qk_code(float v, float sc) {
+  if (sc == 0.0f) return 0;
+  float r = rintf(__fdiv_rn(v, sc));
+  r = fminf(fmaxf(r, -127.0f), 127.0f);
+  return static_cast<int>(r);
+}
+
+template <typename CodeT>
+struct CodeStore;
+
+template <>
+struct CodeStore<int8_t> {
+  // 8 codes -> 8 bytes
+  __device__ static void store(int8_t* dst, const int (&c)[8]) {
+    uint32_t lo = (c[0] & 0xFF) | ((c[1] & 0xFF) << 8) | ((c[2] & 0xFF) << 16) |
+                  (static_cast<uint32_t>(c[3] & 0xFF) << 24);
+    uint32_t hi = (c[4] & 0xFF) | ((c[5] & 0xFF) << 8) | ((c[6] & 0xFF) << 16) |
+                  (static_cast<uint32_t>(c[7] & 0xFF) << 24);
+    *reinterpret_cast<uint2*>(dst) = make_uint2(lo, hi);
+  }
+};
+
+template <>
+struct CodeStore<__half> {
+  // 8 codes -> 8 integer-valued halves (exact for |c| <= 127)
+  __device__ static void store(__half* dst, const int (&c)[8]) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      __half2 h2 = __halves2half2(__int2half_rn(c[2 * i]), __int2half_rn(c[2 * i + 1]));
+      w[i] = *reinterpret_cast<uint32_t*>(&h2);
+    }
+    *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+};
+
+// One warp per (tensor, batch*head, 32-token block).  Lanes 0-15 own channels
+// 8*(lane%16) .. +7 of the even token of a pair, lanes 16-31 of the odd one.
+// grid.y selects Q (0) or K (1).
+template <typename CodeT>
+__global__ void __launch_bounds__(256) qk_quantize_kernel(QKQuantArgs<CodeT> a) {
+  const int tensor = blockIdx.y;
+  const uint16_t* __restrict__ x = tensor == 0 ? a.q : a.k;
+  CodeT* __restrict__ codes = tensor == 0 ? a.q_codes : a.k_codes;
+  float* __restrict__ scale = tensor == 0 ? a.q_scale : a.k_scale;
+
+  const long long gw = static_cast<long long>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32;
+  const int nbp = a.S_pad / 32;
+  if (gw >= static_cast<long long>(a.BH) * nbp) return;
+  const int blk = static_cast<int>(gw % nbp);
+  const int bh = static_cast<int>(gw / nbp);
+  const int b = bh / a.H, h = bh % a.H;
+  const int lane = threadIdx.x & 31;
+  const int half = lane >> 4;
+  const int c8 = (lane & 15) * 8;
+  const size_t tok_stride = static_cast<size_t>(a.H) * kHeadDim;
+  const uint16_t* src = x + (static_cast<size_t>(b) * a.S * a.H + h) * kHeadDim + c8;
+
+  uint4 raw[16];
+  float amax = 0.0f;
+#pragma unroll
+  for (int it = 0; it < 16; ++it) {
+    const int s = blk * 32 + 2 * it + half;
+    raw[it] = s < a.S ? __ldcs(reinterpret_cast<const uint4*>(src + static_cast<size_t>(s) * tok_stride))
+                      : make_uint4(0, 0, 0, 0);
+    const uint32_t w[4] = {raw[it].x, raw[it].y, raw[it].z, raw[it].w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w[i])), fabsf(bf16_hi(w[i]))));
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
+  const float sc = __fdiv_rn(amax, 127.0f);
+  if (lane == 0 && blk < a.nb) scale[static_cast<size_t>(bh) * a.nb + blk] = sc;
+
+  CodeT* dst = codes + (static_cast<size_t>(bh) * a.S_pad + blk * 32 + half) * kHeadDim + c8;
+#pragma unroll
+  for (int it = 0; it < 16; ++it) {
+    const uint32_t w[4] = {raw[it].x, raw[it].y, raw[it].z, raw[it].w};
+    int c[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      c[2 * i] = qk_code(bf16_lo(w[i]), sc);
+      c[2 * i + 1] = qk_code(bf16_hi(w[i]), sc);
+    }
+    CodeStore<CodeT>::store(dst + static_cast<size_t>(2 * it) * kHeadDim, c);
+  }
+}
+
+// Per-channel |v| maxima.  grid = (ceil(S / kVRowsPerCta), B*H), 256 threads;
+// thread t owns channels 8*(t%16) .. +7 of every 16th token.  Results are
+// merged with atomicMax on the fp32 bit patterns (order-preserving for
+// non-negative values) into amax_bits [B*H, 128], which must start at 0.
+constexpr int kVRowsPerCta = 256;
+
+__global__ void __launch_bounds__(256) v_amax_kernel(const uint16_t* __restrict__ v, int S, int H,
+                                                     uint32_t* __restrict__ amax_bits) {
+  __shared__ float part[16][kHeadDim];
+  const int bh = blockIdx.y, b = bh / H, h = bh % H;
+  const int t = threadIdx.x, c8 = (t & 15) * 8, r = t >> 4;
+  const int s0 = blockIdx.x * kVRowsPerCta;
+  const int s1 = min(S, s0 + kVRowsPerCta);
+  const size_t tok_stride = static_cast<size_t>(H) * kHeadDim;
+  const uint16_t* src = v + (static_cast<size_t>(b) * S * H + h) * kHeadDim + c8;
+  float m[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  for (int s = s0 + r; s < s1; s += 16) {
+    const uint4 q = __ldcs(reinterpret_cast<const uint4*>(src + static_cast<size_t>(s) * tok_stride));
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      m[2 * i] = fmaxf(m[2 * i], fabsf(bf16_lo(w[i])));
+      m[2 * i + 1] = fmaxf(m[2 * i + 1], fabsf(bf16_hi(w[i])));
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) part[r][c8 + i] = m[i];
+  __syncthreads();
+  if (t < kHeadDim) {
+    float mm = part[0][t];
+#pragma unroll
+    for (int i = 1; i < 16; ++i) mm = fmaxf(mm, part[i][t]);
+    atomicMax(amax_bits + static_cast<size_t>(bh) * kHeadDim + t, __float_as_uint(mm));
+  }
+}
+
+// Encode one 128-token tile of one (batch, head) and write it transposed.
+// grid = (S_pad / 128, B*H), 256 threads.  Tokens >= S get code 0.
+__global__ void __launch_bounds__(256) v_encode_kernel(const uint16_t* __restrict__ v, int S, int H,
+                                                       int S_pad,
+                                                       const uint32_t* __restrict__ amax_bits,
+                                                       uint8_t* __restrict__ vt,
+                                                       float* __restrict__ v_scale) {
+  constexpr int kPitch = 132;  // bytes per transposed row (word aligned)
+  __shared__ float sv[kHeadDim];
+  __shared__ __align__(16) uint8_t tile[kHeadDim * kPitch];
+  const int bh = blockIdx.y, b = bh / H, h = bh % H;
+  const int tok0 = blockIdx.x * 128;
+  const int t = threadIdx.x;
+  if (t < kHeadDim) {
+    const float s = __fdiv_rn(__uint_as_float(amax_bits[static_cast<size_t>(bh) * kHeadDim + t]), 448.0f);
+    sv[t] = s;
+    if (blockIdx.x == 0) v_scale[static_cast<size_t>(bh) * kHeadDim + t] = s;
+  }
+  __syncthreads();
+  const size_t tok_stride = static_cast<size_t>(H) * kHeadDim;
+  const uint16_t* src = v + (static_cast<size_t>(b) * S * H + h) * kHeadDim;
+#pragma unroll 2
+  for (int k = 0; k < 8; ++k) {
+    const int chunk = k * 256 + t;
+    const int row = chunk >> 4, c8 = (chunk & 15) * 8;
+    const int s = tok0 + row;
+    uint4 q = make_uint4(0, 0, 0, 0);
+    if (s < S) q = __ldcs(reinterpret_cast<const uint4*>(src + static_cast<size_t>(s) * tok_stride + c8));
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int d = c8 + 2 * i;
+      const float y0 = sv[d] == 0.0f ? 0.0f : __fdiv_rn(bf16_lo(w[i]), sv[d]);
+      const float y1 = sv[d + 1] == 0.0f ? 0.0f : __fdiv_rn(bf16_hi(w[i]), sv[d + 1]);
+      const uint16_t pair = cvt_e4m3x2(y0, y1);
+      tile[d * kPitch + row] = static_cast<uint8_t>(pair & 0xFF);
+      tile[(d + 1) * kPitch + row] = static_cast<uint8_t>(pair >> 8);
+    }
+  }
+  __syncthreads();
+  uint8_t* dst = vt + static_cast<size_t>(bh) * kHeadDim * S_pad + tok0;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int chunk = k * 256 + t;
+    const int d = chunk >> 3, c16 = (chunk & 7) * 16;
+    const uint32_t* srow = reinterpret_cast<const uint32_t*>(tile + d * kPitch + c16);
+    *reinterpret_cast<uint4*>(dst + static_cast<size_t>(d) * S_pad + c16) =
+        make_uint4(srow[0], srow[1], srow[2], srow[3]);
+  }
+}
+
+// int8 codes -> integer-valued fp16 codes, 16 per thread.
+__global__ void __launch_bounds__(256) widen_codes_kernel(const int8_t* __restrict__ src,
+                                                          __half* __restrict__ dst, size_t n16) {
+  const size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= n16) return;
+  const int4 q = __ldcs(reinterpret_cast<const int4*>(src) + i);
+  const int w[4] = {q.x, q.y, q.z, q.w};
+  uint32_t o[8];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int lo = static_cast<int8_t>((w[k] >> (16 * j)) & 0xFF);
+      const int hi = static_cast<int8_t>((w[k] >> (16 * j + 8)) & 0xFF);
+      __half2 h2 = __halves2half2(__int2half_rn(lo), __int2half_rn(hi));
+      o[2 * k + j] = *reinterpret_cast<uint32_t*>(&h2);
+    }
+  }
+  uint4* d = reinterpret_cast<uint4*>(dst) + 2 * i;
+  d[0] = make_uint4(o[0], o[1], o[2], o[3]);
+  d[1] = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
+}  // namespace
+
+template <typename CodeT>
+cudaError_t launch_qk_quantize(const QKQuantArgs<CodeT>& a, cudaStream_t stream) {
+  const long long warps = static_cast<long long>(a.BH) * (a.S_pad / 32);
+  const long long ctas = (warps + 7) / 8;
+  qk_quantize_kernel<CodeT><<<dim3(static_cast<unsigned>(ctas), 2), 256, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+template cudaError_t launch_qk_quantize<int8_t>(const QKQuantArgs<int8_t>&, cudaStream_t);
+template cudaError_t launch_qk_quantize<__half>(const QKQuantArgs<__half>&, cudaStream_t);
+
+cudaError_t launch_v_quantize(const uint16_t* v, int B, int S, int H, int S_pad, uint32_t* amax_bits,
+                              uint8_t* vt, float* v_scale, cudaStream_t stream) {
+  const int BH = B * H;
+  cudaError_t e = cudaMemsetAsync(amax_bits, 0, static_cast<size_t>(BH) * kHeadDim * sizeof(uint32_t), stream);
+  if (e != cudaSuccess) return e;
+  v_amax_kernel<<<dim3((S + kVRowsPerCta - 1) / kVRowsPerCta, BH), 256, 0, stream>>>(v, S, H, amax_bits);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  v_encode_kernel<<<dim3(S_pad / 128, BH), 256, 0, stream>>>(v, S, H, S_pad, amax_bits, vt, v_scale);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_widen_codes(const int8_t* src, __half* dst, size_t n, cudaStream_t stream) {
+  const size_t n16 = n / 16;
+  widen_codes_kernel<<<static_cast<unsigned>((n16 + 255) / 256), 256, 0, stream>>>(src, dst, n16);
+  return cudaGetLastError();
+}
+
+}  // namespace sage

@@ -1,0 +1,361 @@
+// sage_api.cu -- the extern "C" boundary: argument checks, workspace layout,
+// stream-ordered scratch, launch sequences and error mapping.  Declarations
+// and their contracts are in include/sage.h.
+#include <atomic>
+#include <cinttypes>
+#include <climits>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "sage.h"
+#include "sage_internal.cuh"
+
+using namespace sage;
+
+namespace {
+
+thread_local std::string t_last_error;
+thread_local cudaEvent_t t_attn_before = nullptr, t_attn_after = nullptr;
+std::atomic<uint64_t> g_timeout_ns{2000000000ull};
+constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
+
+sage_status fail(sage_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  std::vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  t_last_error = buf;
+  return s;
+}
+
+sage_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(SAGE_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+sage_status check_shape(int B, int S, int H, int D) {
+  if (D != kHeadDim)
+    return fail(SAGE_ERR_UNSUPPORTED, "head dimension %d is not supported: this kernel takes D = 128", D);
+  if (B < 1 || S < 1 || H < 1) return fail(SAGE_ERR_INVALID_ARG, "B, S and H must be >= 1 (got %d, %d, %d)", B, S, H);
+  if (static_cast<int64_t>(B) * H > INT_MAX) return fail(SAGE_ERR_INVALID_ARG, "B*H exceeds 2^31-1");
+  if (S > (1 << 28)) return fail(SAGE_ERR_INVALID_ARG, "S = %d exceeds 2^28", S);
+  return SAGE_OK;
+}
+
+sage_status check_scale(float softmax_scale) {
+  if (!std::isfinite(softmax_scale) || !(softmax_scale > 0.0f))
+    return fail(SAGE_ERR_INVALID_ARG, "softmax_scale must be finite and > 0 (got %g)", softmax_scale);
+  return SAGE_OK;
+}
+
+sage_status check_ptrs(std::initializer_list<std::pair<const void*, const char*>> ptrs) {
+  for (auto& pr : ptrs) {
+    if (!pr.first) return fail(SAGE_ERR_INVALID_ARG, "%s is NULL", pr.second);
+    if (!aligned(pr.first, 16)) return fail(SAGE_ERR_MISALIGNED, "%s is not 16-byte aligned", pr.second);
+  }
+  return SAGE_OK;
+}
+
+// Workspace layout (all offsets 256-byte aligned).
+struct WsLayout {
+  size_t q16, k16, vt, qs, ks, vs, vamax, total;
+};
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+WsLayout ws_layout(int B, int S, int H) {
+  const size_t BH = static_cast<size_t>(B) * H, Sp = padded_len(S), nb = num_blocks(S);
+  WsLayout w;
+  size_t off = 0;
+  w.q16 = off; off += align256(BH * Sp * kHeadDim * sizeof(__half));
+  w.k16 = off; off += align256(BH * Sp * kHeadDim * sizeof(__half));
+  w.vt = off; off += align256(BH * kHeadDim * Sp);
+  w.qs = off; off += align256(BH * nb * sizeof(float));
+  w.ks = off; off += align256(BH * nb * sizeof(float));
+  w.vs = off; off += align256(BH * kHeadDim * sizeof(float));
+  w.vamax = off; off += align256(BH * kHeadDim * sizeof(uint32_t));
+  w.total = off;
+  return w;
+}
+
+template <typename T>
+T* at(void* base, size_t off) {
+  return reinterpret_cast<T*>(static_cast<uint8_t*>(base) + off);
+}
+
+// One private stream-ordered pool per device; memory is kept by the pool
+// (release threshold = max) so steady-state calls do not go to the driver.
+std::mutex g_pool_mu;
+cudaMemPool_t g_pools[64] = {};
+
+cudaError_t pool_alloc(void** ptr, size_t bytes, cudaStream_t stream) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  cudaMemPool_t pool;
+  {
+    std::lock_guard<std::mutex> lk(g_pool_mu);
+    if (!g_pools[dev]) {
+      cudaMemPoolProps props;
+      std::memset(&props, 0, sizeof props);
+      props.allocType = cudaMemAllocationTypePinned;
+      props.location.type = cudaMemLocationTypeDevice;
+      props.location.id = dev;
+      e = cudaMemPoolCreate(&g_pools[dev], &props);
+      if (e != cudaSuccess) return e;
+      uint64_t thr = UINT64_MAX;
+      e = cudaMemPoolSetAttribute(g_pools[dev], cudaMemPoolAttrReleaseThreshold, &thr);
+      if (e != cudaSuccess) return e;
+    }
+    pool = g_pools[dev];
+  }
+  return cudaMallocFromPoolAsync(ptr, bytes, pool, stream);
+}
+
+uint64_t timeout_ns() { return g_timeout_ns.load(std::memory_order_relaxed); }
+
+sage_status run_fused(const void* q, const void* k, const void* v, void* out, int B, int S, int H,
+                      float softmax_scale, void* ws, cudaStream_t st) {
+  const WsLayout w = ws_layout(B, S, H);
+  const int Sp = padded_len(S), nb = num_blocks(S);
+  QKQuantArgs<__half> qa;
+  qa.q = static_cast<const uint16_t*>(q);
+  qa.k = static_cast<const uint16_t*>(k);
+  qa.q_codes = at<__half>(ws, w.q16);
+  qa.k_codes = at<__half>(ws, w.k16);
+  qa.q_scale = at<float>(ws, w.qs);
+  qa.k_scale = at<float>(ws, w.ks);
+  qa.BH = B * H;
+  qa.S = S;
+  qa.H = H;
+  qa.S_pad = Sp;
+  qa.nb = nb;
+  cudaError_t e = launch_qk_quantize<__half>(qa, st);
+  if (e != cudaSuccess) return cuda_fail(e, "Q/K quantisation launch");
+  e = launch_v_quantize(static_cast<const uint16_t*>(v), B, S, H, Sp, at<uint32_t>(ws, w.vamax),
+                        at<uint8_t>(ws, w.vt), at<float>(ws, w.vs), st);
+  if (e != cudaSuccess) return cuda_fail(e, "V quantisation launch");
+  AttnArgs aa;
+  aa.q_codes = qa.q_codes;
+  aa.k_codes = qa.k_codes;
+  aa.vt = at<uint8_t>(ws, w.vt);
+  aa.q_scale = qa.q_scale;
+  aa.k_scale = qa.k_scale;
+  aa.v_scale = at<float>(ws, w.vs);
+  aa.out = static_cast<uint16_t*>(out);
+  aa.s_dump = nullptr;
+  aa.B = B;
+  aa.S = S;
+  aa.H = H;
+  aa.S_pad = Sp;
+  aa.nb = nb;
+  aa.softmax_scale = softmax_scale;
+  aa.timeout_ns = timeout_ns();
+  if (t_attn_before && (e = cudaEventRecord(t_attn_before, st)) != cudaSuccess)
+    return cuda_fail(e, "timing event record");
+  e = launch_attention(aa, st);
+  if (e != cudaSuccess) return cuda_fail(e, "attention launch");
+  if (t_attn_after && (e = cudaEventRecord(t_attn_after, st)) != cudaSuccess)
+    return cuda_fail(e, "timing event record");
+  return SAGE_OK;
+}
+
+sage_status run_quantized(const int8_t* q_i8, const float* q_scale, const int8_t* k_i8,
+                          const float* k_scale, const uint8_t* vt, const float* v_scale, void* out,
+                          int32_t* s_dump, int B, int S, int H, float softmax_scale, void* ws,
+                          cudaStream_t st) {
+  const WsLayout w = ws_layout(B, S, H);
+  const int Sp = padded_len(S);
+  const size_t n = static_cast<size_t>(B) * H * Sp * kHeadDim;
+  cudaError_t e = launch_widen_codes(q_i8, at<__half>(ws, w.q16), n, st);
+  if (e == cudaSuccess) e = launch_widen_codes(k_i8, at<__half>(ws, w.k16), n, st);
+  if (e != cudaSuccess) return cuda_fail(e, "code widening launch");
+  AttnArgs aa;
+  aa.q_codes = at<__half>(ws, w.q16);
+  aa.k_codes = at<__half>(ws, w.k16);
+  aa.vt = vt;
+  aa.q_scale = q_scale;
+  aa.k_scale = k_scale;
+  aa.v_scale = v_scale;
+  aa.out = static_cast<uint16_t*>(out);
+  aa.s_dump = s_dump;
+  aa.B = B;
+  aa.S = S;
+  aa.H = H;
+  aa.S_pad = Sp;
+  aa.nb = num_blocks(S);
+  aa.softmax_scale = softmax_scale;
+  aa.timeout_ns = timeout_ns();
+  e = launch_attention(aa, st);
+  if (e != cudaSuccess) return cuda_fail(e, "attention launch");
+  return SAGE_OK;
+}
+
+sage_status check_workspace(void* ws, size_t bytes, int B, int S, int H) {
+  const size_t need = ws_layout(B, S, H).total;
+  if (!ws) return fail(SAGE_ERR_INVALID_ARG, "workspace is NULL");
+  if (!aligned(ws, 256)) return fail(SAGE_ERR_MISALIGNED, "workspace is not 256-byte aligned");
+  if (bytes < need)
+    return fail(SAGE_ERR_WORKSPACE, "workspace of %zu bytes is smaller than the %zu bytes needed", bytes, need);
+  return SAGE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int64_t sage_padded_len(int S) { return S < 1 ? 0 : static_cast<int64_t>(padded_len(S)); }
+
+size_t sage_workspace_bytes(int B, int S, int H, int D) {
+  if (D != kHeadDim || B < 1 || S < 1 || H < 1 || static_cast<int64_t>(B) * H > INT_MAX || S > (1 << 28))
+    return 0;
+  return ws_layout(B, S, H).total;
+}
+
+sage_status sage_quantize_qkv(const void* q, const void* k, const void* v, int B, int S, int H, int D,
+                              int8_t* q_i8, float* q_scale, int8_t* k_i8, float* k_scale,
+                              uint8_t* vt_fp8, float* v_scale, void* stream) {
+  sage_status s = check_shape(B, S, H, D);
+  if (s == SAGE_OK)
+    s = check_ptrs({{q, "q"}, {k, "k"}, {v, "v"}, {q_i8, "q_i8"}, {q_scale, "q_scale"}, {k_i8, "k_i8"},
+                    {k_scale, "k_scale"}, {vt_fp8, "vt_fp8"}, {v_scale, "v_scale"}});
+  if (s != SAGE_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int Sp = padded_len(S), nb = num_blocks(S);
+  QKQuantArgs<int8_t> qa;
+  qa.q = static_cast<const uint16_t*>(q);
+  qa.k = static_cast<const uint16_t*>(k);
+  qa.q_codes = q_i8;
+  qa.k_codes = k_i8;
+  qa.q_scale = q_scale;
+  qa.k_scale = k_scale;
+  qa.BH = B * H;
+  qa.S = S;
+  qa.H = H;
+  qa.S_pad = Sp;
+  qa.nb = nb;
+  cudaError_t e = launch_qk_quantize<int8_t>(qa, st);
+  if (e != cudaSuccess) return cuda_fail(e, "Q/K quantisation launch");
+  void* scratch = nullptr;
+  e = pool_alloc(&scratch, static_cast<size_t>(B) * H * kHeadDim * sizeof(uint32_t), st);
+  if (e != cudaSuccess) return fail(SAGE_ERR_NO_MEMORY, "scratch allocation failed: %s", cudaGetErrorString(e));
+  e = launch_v_quantize(static_cast<const uint16_t*>(v), B, S, H, Sp, static_cast<uint32_t*>(scratch), vt_fp8,
+                        v_scale, st);
+  cudaError_t e2 = cudaFreeAsync(scratch, st);
+  if (e != cudaSuccess) return cuda_fail(e, "V quantisation launch");
+  if (e2 != cudaSuccess) return cuda_fail(e2, "scratch release");
+  return SAGE_OK;
+}
+
+sage_status sage_attn_fwd_ws(const void* q, const void* k, const void* v, void* out, int B, int S,
+                             int H, int D, float softmax_scale, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+  sage_status s = check_shape(B, S, H, D);
+  if (s == SAGE_OK) s = check_scale(softmax_scale);
+  if (s == SAGE_OK) s = check_ptrs({{q, "q"}, {k, "k"}, {v, "v"}, {out, "out"}});
+  if (s == SAGE_OK) s = check_workspace(workspace, workspace_bytes, B, S, H);
+  if (s != SAGE_OK) return s;
+  return run_fused(q, k, v, out, B, S, H, softmax_scale, workspace, static_cast<cudaStream_t>(stream));
+}
+
+sage_status sage_attn_fwd(const void* q, const void* k, const void* v, void* out, int B, int S, int H,
+                          int D, float softmax_scale, void* stream) {
+  sage_status s = check_shape(B, S, H, D);
+  if (s == SAGE_OK) s = check_scale(softmax_scale);
+  if (s == SAGE_OK) s = check_ptrs({{q, "q"}, {k, "k"}, {v, "v"}, {out, "out"}});
+  if (s != SAGE_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  void* ws = nullptr;
+  cudaError_t e = pool_alloc(&ws, ws_layout(B, S, H).total, st);
+  if (e != cudaSuccess)
+    return fail(SAGE_ERR_NO_MEMORY, "workspace allocation of %zu bytes failed: %s", ws_layout(B, S, H).total,
+                cudaGetErrorString(e));
+  s = run_fused(q, k, v, out, B, S, H, softmax_scale, ws, st);
+  e = cudaFreeAsync(ws, st);
+  if (s != SAGE_OK) return s;
+  if (e != cudaSuccess) return cuda_fail(e, "workspace release");
+  return SAGE_OK;
+}
+
+sage_status sage_attn_fwd_quantized(const int8_t* q_i8, const float* q_scale, const int8_t* k_i8,
+                                    const float* k_scale, const uint8_t* vt_fp8,
+                                    const float* v_scale, void* out, int B, int S, int H, int D,
+                                    float softmax_scale, void* workspace, size_t workspace_bytes,
+                                    void* stream) {
+  sage_status s = check_shape(B, S, H, D);
+  if (s == SAGE_OK) s = check_scale(softmax_scale);
+  if (s == SAGE_OK)
+    s = check_ptrs({{q_i8, "q_i8"}, {q_scale, "q_scale"}, {k_i8, "k_i8"}, {k_scale, "k_scale"},
+                    {vt_fp8, "vt_fp8"}, {v_scale, "v_scale"}, {out, "out"}});
+  if (s == SAGE_OK) s = check_workspace(workspace, workspace_bytes, B, S, H);
+  if (s != SAGE_OK) return s;
+  return run_quantized(q_i8, q_scale, k_i8, k_scale, vt_fp8, v_scale, out, nullptr, B, S, H, softmax_scale,
+                       workspace, static_cast<cudaStream_t>(stream));
+}
+
+sage_status sage_debug_qk_int32(const int8_t* q_i8, const float* q_scale, const int8_t* k_i8,
+                                const float* k_scale, const uint8_t* vt_fp8, const float* v_scale,
+                                void* out, int32_t* s_out, int B, int S, int H, int D,
+                                float softmax_scale, void* workspace, size_t workspace_bytes,
+                                void* stream) {
+  sage_status s = check_shape(B, S, H, D);
+  if (s == SAGE_OK) s = check_scale(softmax_scale);
+  if (s == SAGE_OK)
+    s = check_ptrs({{q_i8, "q_i8"}, {q_scale, "q_scale"}, {k_i8, "k_i8"}, {k_scale, "k_scale"},
+                    {vt_fp8, "vt_fp8"}, {v_scale, "v_scale"}, {out, "out"}, {s_out, "s_out"}});
+  if (s == SAGE_OK) s = check_workspace(workspace, workspace_bytes, B, S, H);
+  if (s != SAGE_OK) return s;
+  return run_quantized(q_i8, q_scale, k_i8, k_scale, vt_fp8, v_scale, out, s_out, B, S, H, softmax_scale,
+                       workspace, static_cast<cudaStream_t>(stream));
+}
+
+sage_status sage_debug_wait_timeout(uint64_t ns, void* stream) {
+  if (ns < 1 || ns > 10000000000ull) return fail(SAGE_ERR_INVALID_ARG, "timeout_ns must be in [1, 1e10]");
+  cudaError_t e = launch_wait_timeout_probe(ns, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "wait probe launch");
+  return SAGE_OK;
+}
+
+sage_status sage_sync_status(void* stream) {
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, "stream synchronise");
+  int code = 0;
+  e = read_and_clear_device_error(&code, st);
+  if (e != cudaSuccess) return cuda_fail(e, "device error word read");
+  if (code == SAGE_DEVERR_TIMEOUT)
+    return fail(SAGE_ERR_TIMEOUT, "a device-side wait gave up after its time limit");
+  return SAGE_OK;
+}
+
+void sage_set_attention_events(void* before, void* after) {
+  t_attn_before = static_cast<cudaEvent_t>(before);
+  t_attn_after = static_cast<cudaEvent_t>(after);
+}
+
+void sage_set_wait_timeout_ns(uint64_t ns) { g_timeout_ns.store(ns ? ns : kDefaultTimeoutNs); }
+
+const char* sage_last_error(void) { return t_last_error.c_str(); }
+
+const char* sage_status_string(sage_status s) {
+  switch (s) {
+    case SAGE_OK: return "SAGE_OK";
+    case SAGE_ERR_INVALID_ARG: return "SAGE_ERR_INVALID_ARG";
+    case SAGE_ERR_UNSUPPORTED: return "SAGE_ERR_UNSUPPORTED";
+    case SAGE_ERR_MISALIGNED: return "SAGE_ERR_MISALIGNED";
+    case SAGE_ERR_CUDA: return "SAGE_ERR_CUDA";
+    case SAGE_ERR_NO_MEMORY: return "SAGE_ERR_NO_MEMORY";
+    case SAGE_ERR_TIMEOUT: return "SAGE_ERR_TIMEOUT";
+    case SAGE_ERR_WORKSPACE: return "SAGE_ERR_WORKSPACE";
+  }
+  return "SAGE_ERR_UNKNOWN";
+}
+
+}  // extern "C"

@@ -1,0 +1,64 @@
+// sage_internal.cuh -- declarations shared by the library's translation units
+// (kernel launchers and their argument blocks).  Not part of the public ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+namespace sage {
+
+constexpr int kHeadDim = 128;   // the only head dimension the method takes
+constexpr int kQKBlock = 32;    // tokens per Q/K quantisation block
+constexpr int kTile = 128;      // query rows per Q tile and keys per KV tile
+
+// Device error word codes (read back by the host after a stream sync).
+enum : int { SAGE_DEVERR_NONE = 0, SAGE_DEVERR_TIMEOUT = 1 };
+
+inline int padded_len(int S) { return (S + kTile - 1) / kTile * kTile; }
+inline int num_blocks(int S) { return (S + kQKBlock - 1) / kQKBlock; }
+
+template <typename CodeT>
+struct QKQuantArgs {
+  const uint16_t* q;   // bf16 [B, S, H, 128]
+  const uint16_t* k;
+  CodeT* q_codes;      // [B, H, S_pad, 128]
+  CodeT* k_codes;
+  float* q_scale;      // [B, H, nb]
+  float* k_scale;
+  int BH, S, H, S_pad, nb;
+};
+
+template <typename CodeT>
+cudaError_t launch_qk_quantize(const QKQuantArgs<CodeT>& a, cudaStream_t stream);
+
+// V channel maxima (amax_bits [B*H*128], zeroed here) then E4M3 V^T codes.
+cudaError_t launch_v_quantize(const uint16_t* v, int B, int S, int H, int S_pad, uint32_t* amax_bits,
+                              uint8_t* vt, float* v_scale, cudaStream_t stream);
+
+cudaError_t launch_widen_codes(const int8_t* src, __half* dst, size_t n, cudaStream_t stream);
+
+struct AttnArgs {
+  const __half* q_codes;    // integer-valued fp16 codes [B, H, S_pad, 128]
+  const __half* k_codes;
+  const uint8_t* vt;        // e4m3 V^T [B, H, 128, S_pad]
+  const float* q_scale;     // [B, H, nb]
+  const float* k_scale;
+  const float* v_scale;     // [B, H, 128]
+  uint16_t* out;            // bf16 [B, S, H, 128]
+  int32_t* s_dump;          // optional int32 Q K^T [B, H, S, S] (debug entry only)
+  int B, S, H, S_pad, nb;
+  float softmax_scale;
+  uint64_t timeout_ns;
+};
+
+// Encodes the three TMA maps and launches the fused attention kernel.
+cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream);
+
+// Device error word helpers (per device; set by bounded waits).
+cudaError_t read_and_clear_device_error(int* code, cudaStream_t stream);
+cudaError_t launch_wait_timeout_probe(uint64_t timeout_ns, cudaStream_t stream);
+
+}  // namespace sage

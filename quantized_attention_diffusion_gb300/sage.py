@@ -1,0 +1,250 @@
+"""Thin ctypes binding over ``libsage.so`` (declared in ``include/sage.h``).
+
+The binding marshals torch tensors into pointers, sizes and the current CUDA
+stream; every step of the computation runs in the library's CUDA kernels.
+There is no fallback: if the library is missing or a call fails, a
+``SageError`` is raised.
+
+Accepted inputs mirror the kernel contract of diffusers issue #15014
+("gfx1201 (RDNA4) SageAttention attention backend", kernel contract bullets):
+BF16 Q/K/V of equal shape [B, S, H, 128], no mask, non-causal.  Anything else
+(another dtype, head dim, layout or device) is rejected with a clear error, as
+that issue's "Describe the solution you'd like" asks.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libsage.so")
+HEAD_DIM = 128
+
+_STATUS = {
+    0: "SAGE_OK", 1: "SAGE_ERR_INVALID_ARG", 2: "SAGE_ERR_UNSUPPORTED", 3: "SAGE_ERR_MISALIGNED",
+    4: "SAGE_ERR_CUDA", 5: "SAGE_ERR_NO_MEMORY", 6: "SAGE_ERR_TIMEOUT", 7: "SAGE_ERR_WORKSPACE",
+}
+EXPORTED = (
+    "sage_padded_len", "sage_workspace_bytes", "sage_quantize_qkv", "sage_attn_fwd",
+    "sage_attn_fwd_ws", "sage_attn_fwd_quantized", "sage_debug_qk_int32",
+    "sage_debug_wait_timeout", "sage_sync_status", "sage_set_wait_timeout_ns",
+    "sage_last_error", "sage_status_string", "sage_set_attention_events",
+)
+
+
+class SageError(RuntimeError):
+    """A non-zero sage_status, with the library's message."""
+
+    def __init__(self, status: int, message: str):
+        self.status = status
+        self.name = _STATUS.get(status, f"status {status}")
+        super().__init__(f"{self.name}: {message}")
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load_library(path: str = LIB_PATH):
+    """Load libsage.so and declare its signatures (no CUDA call is made)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"{path} is missing: build it with `python -m quantized_attention_diffusion_gb300.build`")
+        lib = ctypes.CDLL(path)
+        P, I, F, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        S = ctypes.c_int
+        sigs = {
+            "sage_padded_len": (ctypes.c_int64, [I]),
+            "sage_workspace_bytes": (Z, [I, I, I, I]),
+            "sage_quantize_qkv": (S, [P, P, P, I, I, I, I, P, P, P, P, P, P, P]),
+            "sage_attn_fwd": (S, [P, P, P, P, I, I, I, I, F, P]),
+            "sage_attn_fwd_ws": (S, [P, P, P, P, I, I, I, I, F, P, Z, P]),
+            "sage_attn_fwd_quantized": (S, [P, P, P, P, P, P, P, I, I, I, I, F, P, Z, P]),
+            "sage_debug_qk_int32": (S, [P, P, P, P, P, P, P, P, I, I, I, I, F, P, Z, P]),
+            "sage_debug_wait_timeout": (S, [ctypes.c_uint64, P]),
+            "sage_sync_status": (S, [P]),
+            "sage_set_wait_timeout_ns": (None, [ctypes.c_uint64]),
+            "sage_set_attention_events": (None, [P, P]),
+            "sage_last_error": (ctypes.c_char_p, []),
+            "sage_status_string": (ctypes.c_char_p, [S]),
+        }
+        for name, (res, args) in sigs.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+        return lib
+
+
+def _check(status: int):
+    if status != 0:
+        msg = _lib.sage_last_error().decode(errors="replace")
+        raise SageError(status, msg)
+
+
+def _stream(device: torch.device):
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _ptr(t: torch.Tensor | None):
+    return ctypes.c_void_p(0 if t is None else t.data_ptr())
+
+
+def _check_qkv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor):
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor):
+            raise TypeError(f"{name} must be a torch.Tensor")
+        if t.dtype != torch.bfloat16:
+            raise ValueError(f"{name} must be bfloat16 (got {t.dtype})")
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if t.dim() != 4:
+            raise ValueError(f"{name} must be [B, S, H, D] (got {tuple(t.shape)})")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous in [B, S, H, D] order")
+    if not (q.shape == k.shape == v.shape):
+        raise ValueError(f"Q, K and V must have equal shapes (got {tuple(q.shape)}, "
+                         f"{tuple(k.shape)}, {tuple(v.shape)})")
+    if not (q.device == k.device == v.device):
+        raise ValueError("Q, K and V must be on one device")
+    B, S, H, D = q.shape
+    return B, S, H, D
+
+
+def padded_len(S: int) -> int:
+    return int(load_library().sage_padded_len(S))
+
+
+def workspace_bytes(B: int, S: int, H: int, D: int = HEAD_DIM) -> int:
+    return int(load_library().sage_workspace_bytes(B, S, H, D))
+
+
+def attn_fwd(q, k, v, softmax_scale: float | None = None, out=None, workspace=None):
+    """Quantized attention forward: bf16 [B, S, H, 128] -> bf16 [B, S, H, 128].
+
+    ``workspace`` (optional uint8 CUDA tensor of >= workspace_bytes) selects
+    sage_attn_fwd_ws; otherwise the library's stream-ordered pool is used.
+    """
+    lib = load_library()
+    B, S, H, D = _check_qkv(q, k, v)
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q)
+    with torch.cuda.device(q.device):
+        st = _stream(q.device)
+        if workspace is None:
+            _check(lib.sage_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, S, H, D,
+                                     float(softmax_scale), st))
+        else:
+            _check(lib.sage_attn_fwd_ws(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, S, H, D,
+                                        float(softmax_scale), _ptr(workspace),
+                                        workspace.numel() * workspace.element_size(), st))
+    return out
+
+
+def quantize_qkv(q, k, v):
+    """Returns (q_i8 [B,H,S_pad,D], q_scale [B,H,nb], k_i8, k_scale,
+    vt_fp8 uint8 [B,H,D,S_pad], v_scale [B,H,D])."""
+    lib = load_library()
+    B, S, H, D = _check_qkv(q, k, v)
+    Sp = padded_len(S)
+    nb = (S + 31) // 32
+    dev = q.device
+    q_i8 = torch.empty((B, H, Sp, D), dtype=torch.int8, device=dev)
+    k_i8 = torch.empty_like(q_i8)
+    q_sc = torch.empty((B, H, nb), dtype=torch.float32, device=dev)
+    k_sc = torch.empty_like(q_sc)
+    vt = torch.empty((B, H, D, Sp), dtype=torch.uint8, device=dev)
+    v_sc = torch.empty((B, H, D), dtype=torch.float32, device=dev)
+    with torch.cuda.device(dev):
+        _check(lib.sage_quantize_qkv(_ptr(q), _ptr(k), _ptr(v), B, S, H, D, _ptr(q_i8), _ptr(q_sc),
+                                     _ptr(k_i8), _ptr(k_sc), _ptr(vt), _ptr(v_sc), _stream(dev)))
+    return q_i8, q_sc, k_i8, k_sc, vt, v_sc
+
+
+def _quant_shape(q_i8, S):
+    B, H, Sp, D = q_i8.shape
+    if q_i8.dtype != torch.int8 or not q_i8.is_cuda or not q_i8.is_contiguous():
+        raise ValueError("q_i8 must be a contiguous int8 CUDA tensor [B, H, S_pad, D]")
+    if Sp != padded_len(S):
+        raise ValueError(f"S_pad {Sp} does not match S {S}")
+    return B, H, D
+
+
+def attn_fwd_quantized(quant, S: int, softmax_scale: float, out=None, workspace=None,
+                       s_out=None):
+    """Attention from sage_quantize_qkv outputs.  quant = (q_i8, q_scale,
+    k_i8, k_scale, vt_fp8, v_scale).  With ``s_out`` (int32 [B,H,S,S]) the
+    debug entry also dumps the integer QK^T accumulators."""
+    lib = load_library()
+    q_i8, q_sc, k_i8, k_sc, vt, v_sc = quant
+    B, H, D = _quant_shape(q_i8, S)
+    dev = q_i8.device
+    if out is None:
+        out = torch.empty((B, S, H, D), dtype=torch.bfloat16, device=dev)
+    if workspace is None:
+        workspace = torch.empty(workspace_bytes(B, S, H, D), dtype=torch.uint8, device=dev)
+    nbytes = workspace.numel() * workspace.element_size()
+    with torch.cuda.device(dev):
+        st = _stream(dev)
+        if s_out is None:
+            _check(lib.sage_attn_fwd_quantized(_ptr(q_i8), _ptr(q_sc), _ptr(k_i8), _ptr(k_sc),
+                                               _ptr(vt), _ptr(v_sc), _ptr(out), B, S, H, D,
+                                               float(softmax_scale), _ptr(workspace), nbytes, st))
+        else:
+            _check(lib.sage_debug_qk_int32(_ptr(q_i8), _ptr(q_sc), _ptr(k_i8), _ptr(k_sc),
+                                           _ptr(vt), _ptr(v_sc), _ptr(out), _ptr(s_out), B, S, H,
+                                           D, float(softmax_scale), _ptr(workspace), nbytes, st))
+    return out
+
+
+def debug_qk_int32(quant, S: int, softmax_scale: float):
+    """(out bf16 [B,S,H,D], s int32 [B,H,S,S]) from the debug entry point."""
+    q_i8 = quant[0]
+    B, H, _, D = q_i8.shape
+    s_out = torch.empty((B, H, S, S), dtype=torch.int32, device=q_i8.device)
+    out = attn_fwd_quantized(quant, S, softmax_scale, s_out=s_out)
+    return out, s_out
+
+
+def debug_wait_timeout(timeout_ns: int, device=None):
+    """Launch the bounded-wait probe; returns the status sync_status() reports."""
+    lib = load_library()
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(dev):
+        st = _stream(dev)
+        _check(lib.sage_debug_wait_timeout(int(timeout_ns), st))
+        return int(lib.sage_sync_status(st))
+
+
+def sync_status(device=None) -> int:
+    """Synchronise the current stream and return (and clear) the device error status."""
+    lib = load_library()
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(dev):
+        return int(lib.sage_sync_status(_stream(dev)))
+
+
+def set_wait_timeout_ns(ns: int):
+    load_library().sage_set_wait_timeout_ns(int(ns))
+
+
+def set_attention_events(before=None, after=None):
+    """Install (or with no arguments clear) the attention-kernel timing hook.
+
+    ``before``/``after`` are ``torch.cuda.Event`` objects that have been
+    recorded at least once (so that their CUDA handles exist)."""
+    lib = load_library()
+    if before is None or after is None:
+        lib.sage_set_attention_events(None, None)
+    else:
+        lib.sage_set_attention_events(ctypes.c_void_p(before.cuda_event), ctypes.c_void_p(after.cuda_event))

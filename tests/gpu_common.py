@@ -1,0 +1,82 @@
+"""Helpers shared by the GPU parity tests (no test functions here)."""
+import math
+
+import numpy as np
+import torch
+
+import oracle
+from quantized_attention_diffusion_gb300 import build as qbuild
+from quantized_attention_diffusion_gb300.workloads import bf16_bits, make_qkv
+
+# Output tolerance against the oracle: 2e-2 absolute, but never less than one
+# BF16 ulp of the expected value (the kernel and the oracle agree to ~1e-5
+# relative before the final BF16 rounding, so they may round to neighbouring
+# BF16 values), plus the row's tie bound from the oracle (P codes on an E4M3
+# rounding midpoint may round either way).  Accuracy bar against float64
+# unquantized attention: cosine >= 0.999 (the 0.9993 the pages report
+# against SDPA, rounded down to three digits).
+OUT_ATOL = 2e-2
+COS_BAR = 0.999
+
+
+def ensure_library():
+    qbuild.build()
+    import quantized_attention_diffusion_gb300 as qad
+    return qad.load_library()
+
+
+def to_dev(bits: np.ndarray, dtype=torch.bfloat16):
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(dtype)
+    return t.cuda()
+
+
+def f32(bits):
+    return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+def bf16_out_to_f32(t: torch.Tensor) -> np.ndarray:
+    return t.float().cpu().numpy()
+
+
+def cosine(a, b):
+    a = np.asarray(a, dtype=np.float64).ravel()
+    b = np.asarray(b, dtype=np.float64).ravel()
+    return float(a @ b / (np.linalg.norm(a) * np.linalg.norm(b)))
+
+
+def gen(B, S, H, recipe="normal", seed=0):
+    """(cpu bf16 tensors, bf16 bit arrays) for one synthetic workload."""
+    q, k, v = make_qkv(B, S, H, recipe=recipe, seed=seed)
+    return (q, k, v), [bf16_bits(t) for t in (q, k, v)]
+
+
+def quant_to_dev(quant):
+    qc, qs, kc, ks, vt, vs = quant
+    return (torch.from_numpy(qc).cuda(), torch.from_numpy(qs).cuda(), torch.from_numpy(kc).cuda(),
+            torch.from_numpy(ks).cuda(), torch.from_numpy(vt).cuda(), torch.from_numpy(vs).cuda())
+
+
+def default_scale(D=128):
+    return 1.0 / math.sqrt(D)
+
+
+def bf16_ulp(x):
+    a = np.abs(np.asarray(x, dtype=np.float64))
+    e = np.floor(np.log2(np.maximum(a, 2.0 ** -126)))
+    return np.exp2(e - 7)
+
+
+def oracle_tolerance(ref, ties):
+    """Per-element bound |gpu - oracle| may reach (see OUT_ATOL)."""
+    return np.maximum(OUT_ATOL, bf16_ulp(ref)) + np.asarray(ties)[..., None]
+
+
+def assert_close_to_oracle(got, ref, ties, what=""):
+    tol = oracle_tolerance(ref, ties)
+    err = np.abs(np.asarray(got, np.float64) - np.asarray(ref, np.float64))
+    bad = err > tol
+    if bad.any():
+        i = np.unravel_index(np.argmax(err - tol), err.shape)
+        raise AssertionError(f"{what}: {int(bad.sum())} outputs beyond tolerance; worst at {i}: "
+                             f"gpu {got[i]} oracle {ref[i]} tol {tol[i]:.4g}")
+    return float(err.max()), int((np.asarray(ties) > 0).sum())
