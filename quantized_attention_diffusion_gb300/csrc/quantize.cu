@@ -63,35 +63,41 @@ struct CodeStore<__half> {
   }
 };
 
-// One warp per (tensor, batch*head, 32-token block).  Lanes 0-15 own channels
-// 8*(lane%16) .. +7 of the even token of a pair, lanes 16-31 of the odd one.
-// grid.y selects Q (0) or K (1).
+// Four warps per (tensor, batch*head, 32-token block); a CTA of 256 threads
+// takes two blocks.  Warp w (0..3 within its block) owns tokens [8w, 8w+8):
+// lanes 0-15 the even token of a pair, lanes 16-31 the odd one, lane%16 owns
+// channels 8*(lane%16) .. +7.  The block max is a warp shuffle then a
+// shared-memory max over the four warps.  grid.y selects Q (0) or K (1).
 template <typename CodeT>
 __global__ void __launch_bounds__(256) qk_quantize_kernel(QKQuantArgs<CodeT> a) {
+  __shared__ float warp_max[8];
   const int tensor = blockIdx.y;
   const uint16_t* __restrict__ x = tensor == 0 ? a.q : a.k;
   CodeT* __restrict__ codes = tensor == 0 ? a.q_codes : a.k_codes;
   float* __restrict__ scale = tensor == 0 ? a.q_scale : a.k_scale;
 
-  const long long gw = static_cast<long long>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int sub = warp >> 2, w4 = warp & 3;
   const int nbp = a.S_pad / 32;
-  if (gw >= static_cast<long long>(a.BH) * nbp) return;
-  const int blk = static_cast<int>(gw % nbp);
-  const int bh = static_cast<int>(gw / nbp);
+  const long long gblk = static_cast<long long>(blockIdx.x) * 2 + sub;
+  const bool active = gblk < static_cast<long long>(a.BH) * nbp;
+  const int blk = active ? static_cast<int>(gblk % nbp) : 0;
+  const int bh = active ? static_cast<int>(gblk / nbp) : 0;
   const int b = bh / a.H, h = bh % a.H;
-  const int lane = threadIdx.x & 31;
   const int half = lane >> 4;
   const int c8 = (lane & 15) * 8;
+  const int tok0 = blk * 32 + w4 * 8 + half;   // this lane's first token; then +2, +4, +6
   const size_t tok_stride = static_cast<size_t>(a.H) * kHeadDim;
   const uint16_t* src = x + (static_cast<size_t>(b) * a.S * a.H + h) * kHeadDim + c8;
 
-  uint4 raw[16];
+  uint4 raw[4];
   float amax = 0.0f;
 #pragma unroll
-  for (int it = 0; it < 16; ++it) {
-    const int s = blk * 32 + 2 * it + half;
-    raw[it] = s < a.S ? __ldcs(reinterpret_cast<const uint4*>(src + static_cast<size_t>(s) * tok_stride))
-                      : make_uint4(0, 0, 0, 0);
+  for (int it = 0; it < 4; ++it) {
+    const int s = tok0 + 2 * it;
+    raw[it] = (active && s < a.S)
+                  ? __ldcs(reinterpret_cast<const uint4*>(src + static_cast<size_t>(s) * tok_stride))
+                  : make_uint4(0, 0, 0, 0);
     const uint32_t w[4] = {raw[it].x, raw[it].y, raw[it].z, raw[it].w};
 #pragma unroll
     for (int i = 0; i < 4; ++i)
@@ -99,12 +105,17 @@ __global__ void __launch_bounds__(256) qk_quantize_kernel(QKQuantArgs<CodeT> a) 
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
+  if (lane == 0) warp_max[warp] = amax;
+  __syncthreads();
+  amax = fmaxf(fmaxf(warp_max[sub * 4], warp_max[sub * 4 + 1]),
+               fmaxf(warp_max[sub * 4 + 2], warp_max[sub * 4 + 3]));
+  if (!active) return;
   const float sc = __fdiv_rn(amax, 127.0f);
-  if (lane == 0 && blk < a.nb) scale[static_cast<size_t>(bh) * a.nb + blk] = sc;
+  if (w4 == 0 && lane == 0 && blk < a.nb) scale[static_cast<size_t>(bh) * a.nb + blk] = sc;
 
-  CodeT* dst = codes + (static_cast<size_t>(bh) * a.S_pad + blk * 32 + half) * kHeadDim + c8;
+  CodeT* dst = codes + (static_cast<size_t>(bh) * a.S_pad + tok0) * kHeadDim + c8;
 #pragma unroll
-  for (int it = 0; it < 16; ++it) {
+  for (int it = 0; it < 4; ++it) {
     const uint32_t w[4] = {raw[it].x, raw[it].y, raw[it].z, raw[it].w};
     int c[8];
 #pragma unroll
@@ -230,8 +241,8 @@ __global__ void __launch_bounds__(256) widen_codes_kernel(const int8_t* __restri
 
 template <typename CodeT>
 cudaError_t launch_qk_quantize(const QKQuantArgs<CodeT>& a, cudaStream_t stream) {
-  const long long warps = static_cast<long long>(a.BH) * (a.S_pad / 32);
-  const long long ctas = (warps + 7) / 8;
+  const long long blocks = static_cast<long long>(a.BH) * (a.S_pad / 32);
+  const long long ctas = (blocks + 1) / 2;
   qk_quantize_kernel<CodeT><<<dim3(static_cast<unsigned>(ctas), 2), 256, 0, stream>>>(a);
   return cudaGetLastError();
 }
