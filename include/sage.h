@@ -87,6 +87,32 @@ sage_status sage_quantize_qkv(const void* q, const void* k, const void* v, int B
                               uint8_t* vt_fp8, float* v_scale, void* stream);
 
 /*
+ * sage_quantize_qkv_noalloc -- sage_quantize_qkv for callers that cannot
+ * allocate device memory.  No counterpart on the pages.
+ *
+ * Some callers cannot call cudaMalloc or any allocating routine where they
+ * quantise: code running under a framework that owns every device
+ * allocation, a real-time loop that must not take the driver's allocation
+ * locks, or a device whose memory was reserved up front.  sage_quantize_qkv
+ * takes its scratch (the per-channel |V| maxima, 4 * B * H * 128 bytes) from
+ * a stream-ordered pool; this entry point uses a fixed 4 MiB array in device
+ * memory instead and allocates nothing (it calls no cudaMalloc, no pool
+ * allocation, no allocating library routine).
+ *
+ * Same arguments, outputs, layouts and results as sage_quantize_qkv.  Limit:
+ * B * H <= 8192, else SAGE_ERR_INVALID_ARG with a message.  The array lives in
+ * every GPU that loads this library until the process exits.  The first call
+ * on a device looks up the array's device address (cudaGetSymbolAddress, with
+ * that device current); make that first call before any stream capture.
+ * Every call shares the array, which keeps the last call's contents; each call
+ * zeroes the part it uses first.  Calls whose work overlaps on the GPU (on
+ * different streams, or on other host threads) race on the array: order them.
+ */
+sage_status sage_quantize_qkv_noalloc(const void* q, const void* k, const void* v, int B, int S,
+                                      int H, int D, int8_t* q_i8, float* q_scale, int8_t* k_i8,
+                                      float* k_scale, uint8_t* vt_fp8, float* v_scale, void* stream);
+
+/*
  * sage_attn_fwd -- the whole path: quantise Q/K/V, then fused quantized
  * attention.  Passage: the issue's contract bullets (INT8 QK^T, FP8 PV,
  * FP32 accumulation; BF16 [B, S, H, 128]; no mask, non-causal) and

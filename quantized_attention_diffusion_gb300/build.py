@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "libsage.so")
 INCLUDE = os.path.join(ROOT, "include")
-SOURCES = ["sage_api.cu", "quantize.cu", "attention.cu"]
+SOURCES = ["sage_api.cu", "quantize.cu", "attention.cu", "quantize_noalloc.cu"]
 HEADERS = ["sage_internal.cuh", "sm103_ptx.cuh"]
 
 NVCC_FLAGS = [

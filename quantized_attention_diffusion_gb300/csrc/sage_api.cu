@@ -209,6 +209,15 @@ sage_status check_workspace(void* ws, size_t bytes, int B, int S, int H) {
 
 }  // namespace
 
+void sage::set_last_error(const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  std::vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  t_last_error = buf;
+}
+
 extern "C" {
 
 int64_t sage_padded_len(int S) { return S < 1 ? 0 : static_cast<int64_t>(padded_len(S)); }

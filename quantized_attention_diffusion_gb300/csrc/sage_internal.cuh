@@ -57,6 +57,9 @@ struct AttnArgs {
 // Encodes the three TMA maps and launches the fused attention kernel.
 cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream);
 
+// Records printf-style text as this thread's sage_last_error() message.
+void set_last_error(const char* fmt, ...);
+
 // Device error word helpers (per device; set by bounded waits).
 cudaError_t read_and_clear_device_error(int* code, cudaStream_t stream);
 cudaError_t launch_wait_timeout_probe(uint64_t timeout_ns, cudaStream_t stream);

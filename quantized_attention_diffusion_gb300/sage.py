@@ -33,6 +33,7 @@ EXPORTED = (
     "sage_attn_fwd_ws", "sage_attn_fwd_quantized", "sage_debug_qk_int32",
     "sage_debug_wait_timeout", "sage_sync_status", "sage_set_wait_timeout_ns",
     "sage_last_error", "sage_status_string", "sage_set_attention_events",
+    "sage_quantize_qkv_noalloc",
 )
 
 
@@ -65,6 +66,7 @@ def load_library(path: str = LIB_PATH):
             "sage_padded_len": (ctypes.c_int64, [I]),
             "sage_workspace_bytes": (Z, [I, I, I, I]),
             "sage_quantize_qkv": (S, [P, P, P, I, I, I, I, P, P, P, P, P, P, P]),
+            "sage_quantize_qkv_noalloc": (S, [P, P, P, I, I, I, I, P, P, P, P, P, P, P]),
             "sage_attn_fwd": (S, [P, P, P, P, I, I, I, I, F, P]),
             "sage_attn_fwd_ws": (S, [P, P, P, P, I, I, I, I, F, P, Z, P]),
             "sage_attn_fwd_quantized": (S, [P, P, P, P, P, P, P, I, I, I, I, F, P, Z, P]),
@@ -151,10 +153,22 @@ def attn_fwd(q, k, v, softmax_scale: float | None = None, out=None, workspace=No
     return out
 
 
-def quantize_qkv(q, k, v):
+def quantize_qkv(q, k, v, out=None, noalloc=False):
     """Returns (q_i8 [B,H,S_pad,D], q_scale [B,H,nb], k_i8, k_scale,
-    vt_fp8 uint8 [B,H,D,S_pad], v_scale [B,H,D])."""
+    vt_fp8 uint8 [B,H,D,S_pad], v_scale [B,H,D]).
+
+    ``out`` (optional) is a tuple of those six tensors to fill.  With
+    ``noalloc`` the call goes to sage_quantize_qkv_noalloc, which uses the
+    library's built-in scratch instead of allocating (B*H <= 8192)."""
     lib = load_library()
+    if out is not None:
+        B, S, H, D = _check_qkv(q, k, v)
+        q_i8, q_sc, k_i8, k_sc, vt, v_sc = out
+        fn = lib.sage_quantize_qkv_noalloc if noalloc else lib.sage_quantize_qkv
+        with torch.cuda.device(q.device):
+            _check(fn(_ptr(q), _ptr(k), _ptr(v), B, S, H, D, _ptr(q_i8), _ptr(q_sc), _ptr(k_i8),
+                      _ptr(k_sc), _ptr(vt), _ptr(v_sc), _stream(q.device)))
+        return out
     B, S, H, D = _check_qkv(q, k, v)
     Sp = padded_len(S)
     nb = (S + 31) // 32
@@ -165,9 +179,10 @@ def quantize_qkv(q, k, v):
     k_sc = torch.empty_like(q_sc)
     vt = torch.empty((B, H, D, Sp), dtype=torch.uint8, device=dev)
     v_sc = torch.empty((B, H, D), dtype=torch.float32, device=dev)
+    fn = lib.sage_quantize_qkv_noalloc if noalloc else lib.sage_quantize_qkv
     with torch.cuda.device(dev):
-        _check(lib.sage_quantize_qkv(_ptr(q), _ptr(k), _ptr(v), B, S, H, D, _ptr(q_i8), _ptr(q_sc),
-                                     _ptr(k_i8), _ptr(k_sc), _ptr(vt), _ptr(v_sc), _stream(dev)))
+        _check(fn(_ptr(q), _ptr(k), _ptr(v), B, S, H, D, _ptr(q_i8), _ptr(q_sc),
+                  _ptr(k_i8), _ptr(k_sc), _ptr(vt), _ptr(v_sc), _stream(dev)))
     return q_i8, q_sc, k_i8, k_sc, vt, v_sc
 
 
