@@ -35,8 +35,8 @@
  *      so that exp(s_j - s_k) = 2^(x_j - x_k) with s = acc * sq * sk *
  *      softmax_scale.  The kernel takes the FP8 decisions of R8 from these
  *      same fp32 values, so both sides decide every P code in one precision.
- *  R7  online softmax in FP32 over KV tiles of 128 keys (keys [128t,
- *      128t+128) that exist): the running max m_t = max(m_{t-1}, max_{j in
+ *  R7  online softmax in FP32 over KV tiles of 96 keys (keys [96t, 96t+96)
+ *      that exist; 96 = three K blocks): the running max m_t = max(m_{t-1}, max_{j in
  *      t} x_j) (m_{-1} = -inf); bias_t = fl(m_t - LOG2_448) with LOG2_448 =
  *      fp32(log2 448); p_j = fp32(2^fmaf(acc_j, cb_j, -bias_t)) (2^ in double,
  *      rounded once), so p_j <= 448 is 448 * exp(s_j - running max);
@@ -215,7 +215,7 @@ int oracle_qk_int32(const int8_t *q, const int8_t *k, int B, int S, int H,
 /* The fp32 value nearest log2(e), and fp32(log2(448)). */
 #define ORACLE_L2E 1.44269502162933349609375f
 #define ORACLE_LOG2_448 8.80735492706298828125f
-#define ORACLE_KV_TILE 128
+#define ORACLE_KV_TILE 96
 #define ORACLE_TIE_REL 1.9073486328125e-06 /* 2^-19 */
 
 /* Distance of an E4M3 code's value to the other side of the nearest rounding

@@ -264,6 +264,17 @@ __device__ __forceinline__ float2 ffma2_bc(float a0, float a1, float b, float c)
   return r;
 }
 
+// (a0, a1) * b on the packed FP32 pipe.
+__device__ __forceinline__ float2 fmul2(float a0, float a1, float b) {
+  float2 r;
+  asm("{\n\t.reg .b64 x, y, w;\n\t"
+      "mov.b64 x, {%2, %3};\n\tmov.b64 y, {%4, %4};\n\t"
+      "mul.rn.f32x2 w, x, y;\n\tmov.b64 {%0, %1}, w;\n\t}"
+      : "=f"(r.x), "=f"(r.y)
+      : "f"(a0), "f"(a1), "f"(b));
+  return r;
+}
+
 // Two E4M3 codes (low byte first) -> their exact values as f16x2.
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t codes) {
   uint32_t h2;

@@ -132,12 +132,12 @@ def _block_preserving_permutation(S, rng, span=None):
 
 
 def test_kv_permutation_within_a_tile_is_exact():
-    """Inside one 128-key tile the max is order-free, the block scales move
+    """Inside one 96-key tile the max is order-free, the block scales move
     with their blocks and the tile's PV sum is exact: bit-identical output."""
-    B, S, H = 1, 256, 2
+    B, S, H = 1, 288, 2
     q, k, v = qkv_bits(B, S, H, seed=14, recipe="k_channel_offset")
     base = oracle.attention(q, k, v, 1 / math.sqrt(128))
-    perm = _block_preserving_permutation(S, np.random.default_rng(14), span=128)
+    perm = _block_preserving_permutation(S, np.random.default_rng(14), span=96)
     out = oracle.attention(q, k[:, perm], v[:, perm], 1 / math.sqrt(128))
     assert np.array_equal(out, base)
 
@@ -173,19 +173,19 @@ def test_kv_arbitrary_permutation_changes_only_quantisation_noise():
 
 
 def test_online_rescale_two_tiles_closed_form():
-    """Tile 0: 128 keys with score s0, tile 1: 70 keys with s1 > s0.  Every P
-    code is 448 against its tile's running max, so L = alpha*128*448 +
-    70*448 with alpha = 2^(x0 - x1) (the fp32 base-2 scores), and with V
-    constant per tile out = (alpha*128*v0 + 70*v1) / (alpha*128 + 70)."""
-    S, D = 198, 128
+    """Tile 0: 96 keys with score s0, tile 1: 70 keys with s1 > s0.  Every P
+    code is 448 against its tile's running max, so L = alpha*96*448 + 70*448
+    with alpha = 2^(x0 - x1) (the fp32 base-2 scores), and with V constant per
+    tile out = (alpha*96*v0 + 70*v1) / (alpha*96 + 70)."""
+    S, D = 166, 128
     q = np.zeros((1, S, 1, D), np.float32)
     k = np.zeros((1, S, 1, D), np.float32)
     v = np.zeros((1, S, 1, D), np.float32)
     q[0, :, 0, 0] = 1.0
-    k[0, :128, 0, 0] = 0.5                  # K blocks of tile 0: scale 0.5/127
-    k[0, 128:, 0, 0] = 1.25                 # K blocks of tile 1: scale 1.25/127
-    v[0, :128, 0, :] = 2.0
-    v[0, 128:, 0, :] = -1.0
+    k[0, :96, 0, 0] = 0.5                   # K blocks of tile 0: scale 0.5/127
+    k[0, 96:, 0, 0] = 1.25                  # K blocks of tile 1: scale 1.25/127
+    v[0, :96, 0, :] = 2.0
+    v[0, 96:, 0, :] = -1.0
     quant = oracle.quantize(bf16(q), bf16(k), bf16(v))
     scale = 1 / math.sqrt(128)
     out, pc, L = oracle.attend_row_debug(quant, S, scale, 0, 0, 5)
@@ -193,14 +193,14 @@ def test_online_rescale_two_tiles_closed_form():
     f = np.float32
     c_row = f(quant[1][0, 0, 0]) * (f(scale) * f(1.4426950408889634))
     x0 = f(16129) * (c_row * quant[3][0, 0, 0])
-    x1 = f(16129) * (c_row * quant[3][0, 0, 4])
+    x1 = f(16129) * (c_row * quant[3][0, 0, 3])
     alpha = float(f(2.0 ** float(f(x0 - x1))))
     assert 0 < alpha < 1
-    assert abs(L - (alpha * 128 * 448 + 70 * 448)) <= 1e-9 * L
+    assert abs(L - (alpha * 96 * 448 + 70 * 448)) <= 1e-9 * L
     sv = float(quant[5][0, 0, 0])
     v0 = oracle.e4m3_decode(quant[4][0, 0, 0, 0]) * sv
-    v1 = oracle.e4m3_decode(quant[4][0, 0, 0, 128]) * sv
-    expect = (alpha * 128 * v0 + 70 * v1) / (alpha * 128 + 70)
+    v1 = oracle.e4m3_decode(quant[4][0, 0, 0, 96]) * sv
+    expect = (alpha * 96 * v0 + 70 * v1) / (alpha * 96 + 70)
     assert np.allclose(f32(out), expect, rtol=2 ** -8, atol=0)
 
 
@@ -235,20 +235,20 @@ def test_row_subset_matches_full():
 
 
 def test_softmax_reading_max_column_is_448_and_fp32_sum():
-    """Within one tile (S <= 128): the max-score key gets code 448, L is the
+    """Within one tile (S <= 96): the max-score key gets code 448, L is the
     sum of the dequantised codes, and the unquantised-sum reading differs by
     at most the E4M3 half-step (2^-4 relative)."""
-    q, k, v = qkv_bits(1, 120, 1, seed=19, recipe="k_channel_offset")
+    q, k, v = qkv_bits(1, 90, 1, seed=19, recipe="k_channel_offset")
     quant = oracle.quantize(q, k, v)
     scale = 1 / math.sqrt(128)
-    s = oracle.qk_int32(quant[0], quant[2], 120)[0, 0].astype(np.float64)
-    for i in (0, 60, 119):
-        _, pc, L = oracle.attend_row_debug(quant, 120, scale, 0, 0, i)
+    s = oracle.qk_int32(quant[0], quant[2], 90)[0, 0].astype(np.float64)
+    for i in (0, 45, 89):
+        _, pc, L = oracle.attend_row_debug(quant, 90, scale, 0, 0, i)
         dec = oracle.e4m3_decode(pc)
-        j = int(np.argmax(s[i] * quant[3][0, 0, np.arange(120) // 32]))
+        j = int(np.argmax(s[i] * quant[3][0, 0, np.arange(90) // 32]))
         assert pc[j] == 0x7E
         assert L == dec.sum() and dec.max() == 448.0
-        _, _, Lp = oracle.attend_row_debug(quant, 120, scale, 0, 0, i, l_mode=1)
+        _, _, Lp = oracle.attend_row_debug(quant, 90, scale, 0, 0, i, l_mode=1)
         assert abs(Lp - L) <= L * 2.0 ** -4
 
 
