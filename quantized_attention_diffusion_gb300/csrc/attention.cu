@@ -23,20 +23,28 @@
 // One CTA owns two 128-row Q tiles of one (batch, head) and streams every KV
 // tile of that head.  384 threads:
 //   warp 0       TMA producer (Q once; K and V^T through 3-stage rings)
-//   warp 1       TMEM allocator and the single MMA-issuing thread
-//   warps 2-3    write the ones rows of the V stages, then idle
+//   warp 1       TMEM allocator; issues the QK^T MMAs (one thread)
+//   warp 2       issues the PV MMAs (one thread)
+//   warps 2-3    first write the ones rows of the V stages
 //   warps 4-7    softmax + epilogue of Q tile 0, one thread per query row
 //   warps 8-11   the same for Q tile 1
 // TMEM (512 columns allocated): S0 [0,96)  S1 [96,192)  O0 [192,336)
 // O1 [336,480).  KV tiles are 96 keys so that two S tiles and two N=144
 // accumulators fit; 96 keys are exactly three K quantisation blocks and
-// three K=32 steps of the PV MMA.  P~ (E4M3, 4 per column) overwrites the
-// first 24 columns of its S tile and is the A operand of PV from TMEM.
+// three K=32 steps of the PV MMA.
 //
-// The two Q tiles ping-pong: the MMA queue runs PV0(j), QK0(j+1), PV1(j),
-// QK1(j+1), so the softmax of one tile overlaps the tensor work of the other,
-// and a tile's next scores exist only once its PV has consumed P~ (which
-// aliases S) and left O final for the next rescale.
+// P~ goes to shared memory (one 128-row, 128-byte-pitch tile per Q tile, in
+// the swizzled layout the MMA descriptors read), not over S.  A softmax
+// thread hands its S columns back as soon as it has loaded them, so QK(j+1)
+// of a tile runs while the softmax of tile j is still computing, and the two
+// issuing threads keep QK and PV apart: QK runs ahead as far as S is free,
+// PV follows P~.  Before writing P~(j) or rescaling O, a softmax thread waits
+// for PV(j-1) of its tile.
+//
+// An M=128 MMA from one thread takes about 48-72 SM clocks here, barely more
+// than one thread needs to issue it, so the issue loops are kept short:
+// descriptors are formed from precomputed lower words, and barrier waits
+// inline only their first poll.
 #include <cmath>
 #include <cstring>
 #include <cuda.h>
@@ -63,10 +71,12 @@ constexpr uint32_t kKTileBytes = 2 * kKHalf;
 constexpr uint32_t kVTileBytes = 128 * 128;              // V^T: 128 channels x 128 keys (96 used)
 constexpr uint32_t kOnesBytes = 16 * 128;                // 16 rows of E4M3 1.0
 constexpr uint32_t kVStageBytes = kVTileBytes + kOnesBytes;
+constexpr uint32_t kPTileBytes = 128 * 128;              // P~: 128 rows x 128 bytes (96 used)
 constexpr uint32_t kSmemQ = 0;
 constexpr uint32_t kSmemK = kSmemQ + 2 * kQTileBytes;
 constexpr uint32_t kSmemV = kSmemK + kStages * kKTileBytes;
-constexpr uint32_t kSmemTiles = kSmemV + kStages * kVStageBytes;
+constexpr uint32_t kSmemP = kSmemV + kStages * kVStageBytes;
+constexpr uint32_t kSmemTiles = kSmemP + 2 * kPTileBytes;
 constexpr uint32_t kSmemDynamic = kSmemTiles + 1024;     // slack for 1024-byte alignment
 // TMEM columns of tile t's scores (96) and accumulator (144; L at +128).
 __host__ __device__ constexpr uint32_t col_s(int t) { return static_cast<uint32_t>(t) * kKV; }
@@ -75,7 +85,7 @@ constexpr float kLog2P = 8.80735492706298828125f;         // fp32(log2 448): P s
 constexpr float kLog2e = 1.44269502162933349609375f;      // fp32(log2 e)
 constexpr uint32_t kE4M3One = 0x38383838u;                // four E4M3 1.0
 
-static_assert(kSmemDynamic <= 227 * 1024 - 2048, "shared memory budget");
+static_assert(kSmemDynamic <= 227 * 1024 - 1024, "shared memory budget");
 
 struct Params {
   const float* q_scale;
@@ -92,8 +102,8 @@ struct Barriers {
   uint64_t q_full;
   uint64_t k_full[kStages], k_empty[kStages];
   uint64_t v_full[kStages], v_empty[kStages];
-  uint64_t s_full[2], p_full[2], o_full[2];
-  uint64_t drain;
+  uint64_t s_full[2], s_free[2], p_full[2], pv_done[2], o_full[2];
+  uint64_t drain_qk, drain_pv;
 };
 
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
@@ -119,31 +129,33 @@ __device__ __forceinline__ void store_bf16x8(uint16_t* dst, const float (&v)[8])
 }
 
 // One row's 96 integer scores -> 96 E4M3 probabilities p~ = e4m3(2^(acc *
-// cb[block] - bias)) in 24 TMEM columns (4 codes per column, key k at column
-// k/4 byte k%4): the A operand of the PV MMA.  kMasked: keys >= valid get 0.
-template <bool kMasked>
+// cb[block] - bias)), four codes per word, key k in byte k%4 of word k/4.
 __device__ __forceinline__ void softmax_p(const float (&a)[kKV], const float (&cb)[3], float bias,
-                                          int valid, uint32_t tP) {
+                                          uint32_t (&pk)[kKV / 4]) {
 #pragma unroll
   for (int blk = 0; blk < 3; ++blk) {
-    uint32_t pk[8];
 #pragma unroll
     for (int w = 0; w < 8; ++w) {
       const int c = blk * 32 + w * 4;
       const float2 x01 = ffma2_bc(a[c], a[c + 1], cb[blk], -bias);
       const float2 x23 = ffma2_bc(a[c + 2], a[c + 3], cb[blk], -bias);
-      float p0 = ex2_approx(x01.x), p1 = ex2_approx(x01.y);
-      float p2 = ex2_approx(x23.x), p3 = ex2_approx(x23.y);
-      if constexpr (kMasked) {
-        p0 = c < valid ? p0 : 0.0f;
-        p1 = c + 1 < valid ? p1 : 0.0f;
-        p2 = c + 2 < valid ? p2 : 0.0f;
-        p3 = c + 3 < valid ? p3 : 0.0f;
-      }
-      pk[w] = static_cast<uint32_t>(cvt_e4m3x2(p0, p1)) | (static_cast<uint32_t>(cvt_e4m3x2(p2, p3)) << 16);
+      const float p0 = ex2_approx(x01.x), p1 = ex2_approx(x01.y);
+      const float p2 = ex2_approx(x23.x), p3 = ex2_approx(x23.y);
+      pk[blk * 8 + w] =
+          static_cast<uint32_t>(cvt_e4m3x2(p0, p1)) | (static_cast<uint32_t>(cvt_e4m3x2(p2, p3)) << 16);
     }
-    tmem_st8(tP + blk * 8, pk);
   }
+}
+
+// Row r of a P~ tile in the 128-byte-swizzled K-major layout: 16-byte chunk
+// c of row r sits at (r/8)*1024 + (r%8)*128 + (c ^ (r%8))*16.  Chunks 0-5
+// hold the 96 codes.
+__device__ __forceinline__ void store_p_row(uint8_t* tile, int r, const uint32_t (&pk)[kKV / 4]) {
+  uint8_t* base = tile + (r >> 3) * 1024 + (r & 7) * 128;
+#pragma unroll
+  for (int c = 0; c < kKV / 16; ++c)
+    *reinterpret_cast<uint4*>(base + ((c ^ (r & 7)) << 4)) =
+        make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
 }
 
 template <bool kDumpS>
@@ -166,6 +178,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sQ = smem + kSmemQ;
   uint8_t* sK = smem + kSmemK;
   uint8_t* sV = smem + kSmemV;
+  uint8_t* sP = smem + kSmemP;
 
   if (threadIdx.x == 0) {
     mbar_init(&bars.q_full, 1);
@@ -177,10 +190,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bars.s_full[t], 1);
+      mbar_init(&bars.s_free[t], 128);
       mbar_init(&bars.p_full[t], 128);
+      mbar_init(&bars.pv_done[t], 1);
       mbar_init(&bars.o_full[t], 1);
     }
-    mbar_init(&bars.drain, 1);
+    mbar_init(&bars.drain_qk, 1);
+    mbar_init(&bars.drain_pv, 1);
     abort_flag = 0;
     fence_mbarrier_init();
     tma_prefetch_desc(&tmQ);
@@ -235,66 +251,67 @@ __global__ void __launch_bounds__(kThreads, 1)
         drain_bar(&bars.v_full[j % kStages], (j / kStages) & 1, p.timeout_ns);
     }
   } else if (warp == 1) {
-    // -------------------------------------------------------- MMA issuer --
+    // ------------------------------------------------------ QK^T issuer --
     if (lane == 0) {
-      const uint32_t idesc_qk = make_idesc_f32acc(128, kKV, 0, 0);   // F16 x F16 -> F32
-      const uint32_t idesc_pv = make_idesc_f32acc(128, 144, 0, 0);   // E4M3 x E4M3 -> F32
-      const uint32_t sq_addr = smem_addr(sQ), sk_addr = smem_addr(sK), sv_addr = smem_addr(sV);
-      auto qk = [&](int t, int s) {   // S_t = Q_t K(s)^T
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-          mma_f16_ss(tmem + col_s(t),
-                     make_sw128_desc(sq_addr + t * kQTileBytes + (k >> 2) * kQHalf + (k & 3) * 32),
-                     make_sw128_desc(sk_addr + s * kKTileBytes + (k >> 2) * kKHalf + (k & 3) * 32),
-                     idesc_qk, k > 0);
-      };
-      auto pv = [&](int t, int s, int j) {   // O_t[0:144] += P~_t [V^T(s); ones]^T
-#pragma unroll
-        for (int k = 0; k < 3; ++k)
-          mma_f8_ts(tmem + col_o(t), tmem + col_s(t) + k * 8,
-                    make_sw128_desc(sv_addr + s * kVStageBytes + k * 32), idesc_pv, (j > 0 || k > 0));
-      };
-      bool ok = wait_bar(&bars.q_full, 0, abort_v, p.timeout_ns) &&
-                wait_bar(&bars.k_full[0], 0, abort_v, p.timeout_ns);
-      if (ok) {
-        tc_fence_after();
-        qk(0, 0);
-        mma_commit(&bars.s_full[0]);
-        qk(1, 0);
-        mma_commit(&bars.s_full[1]);
-        mma_commit(&bars.k_empty[0]);
+      const uint32_t idesc = make_idesc_f32acc(128, kKV, 0, 0);   // F16 x F16 -> F32
+      const uint32_t q_lo = sw128_desc_lo(smem_addr(sQ)), k_lo = sw128_desc_lo(smem_addr(sK));
+      if (wait_bar(&bars.q_full, 0, abort_v, p.timeout_ns)) {
         for (int j = 0; j < p.n_kv; ++j) {
           const int s = j % kStages;
-          const bool more = j + 1 < p.n_kv;
-          const int s2 = (j + 1) % kStages;
-          if (!wait_bar(&bars.v_full[s], (j / kStages) & 1, abort_v, p.timeout_ns)) break;
-          if (!wait_bar(&bars.p_full[0], j & 1, abort_v, p.timeout_ns)) break;
-          tc_fence_after();
-          pv(0, s, j);
-          if (more) {
-            if (!wait_bar(&bars.k_full[s2], ((j + 1) / kStages) & 1, abort_v, p.timeout_ns)) break;
+          if (!wait_bar(&bars.k_full[s], (j / kStages) & 1, abort_v, p.timeout_ns)) break;
+          const uint32_t b0 = k_lo + s * (kKTileBytes >> 4);
+          bool ok = true;
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {   // S_t = Q_t K(j)^T once S_t is free
+            if (j > 0 && !wait_bar(&bars.s_free[t], (j - 1) & 1, abort_v, p.timeout_ns)) {
+              ok = false;
+              break;
+            }
             tc_fence_after();
-            qk(0, s2);
-            mma_commit(&bars.s_full[0]);
-          } else {
-            mma_commit(&bars.o_full[0]);
+            const uint32_t a0 = q_lo + t * (kQTileBytes >> 4);
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              mma_f16_ss(tmem + col_s(t), a0 + (((k >> 2) * kQHalf + (k & 3) * 32) >> 4),
+                         b0 + (((k >> 2) * kKHalf + (k & 3) * 32) >> 4), idesc, k > 0);
+            mma_commit(&bars.s_full[t]);
           }
-          if (!wait_bar(&bars.p_full[1], j & 1, abort_v, p.timeout_ns)) break;
-          tc_fence_after();
-          pv(1, s, j);
-          mma_commit(&bars.v_empty[s]);
-          if (more) {
-            qk(1, s2);
-            mma_commit(&bars.s_full[1]);
-            mma_commit(&bars.k_empty[s2]);
-          } else {
-            mma_commit(&bars.o_full[1]);
-          }
+          if (!ok) break;
+          mma_commit(&bars.k_empty[s]);
         }
       }
       // Wait for every issued MMA before TMEM can be released.
-      mma_commit(&bars.drain);
-      drain_bar(&bars.drain, 0, p.timeout_ns);
+      mma_commit(&bars.drain_qk);
+      drain_bar(&bars.drain_qk, 0, p.timeout_ns);
+    }
+  } else if (warp == 2) {
+    // -------------------------------------------------------- PV issuer --
+    if (lane == 0) {
+      const uint32_t idesc = make_idesc_f32acc(128, 144, 0, 0);   // E4M3 x E4M3 -> F32
+      const uint32_t p_lo = sw128_desc_lo(smem_addr(sP)), v_lo = sw128_desc_lo(smem_addr(sV));
+      for (int j = 0; j < p.n_kv; ++j) {
+        const int s = j % kStages;
+        if (!wait_bar(&bars.v_full[s], (j / kStages) & 1, abort_v, p.timeout_ns)) break;
+        const uint32_t b0 = v_lo + s * (kVStageBytes >> 4);
+        bool ok = true;
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {     // O_t[0:144] += P~_t [V^T(j); ones]^T
+          if (!wait_bar(&bars.p_full[t], j & 1, abort_v, p.timeout_ns)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = p_lo + t * (kPTileBytes >> 4);
+#pragma unroll
+          for (int k = 0; k < 3; ++k) mma_f8_ss(tmem + col_o(t), a0 + 2 * k, b0 + 2 * k, idesc, (j > 0 || k > 0));
+          mma_commit(&bars.pv_done[t]);
+        }
+        if (!ok) break;
+        mma_commit(&bars.v_empty[s]);
+      }
+      mma_commit(&bars.o_full[0]);
+      mma_commit(&bars.o_full[1]);
+      mma_commit(&bars.drain_pv);
+      drain_bar(&bars.drain_pv, 0, p.timeout_ns);
     }
   } else if (warp >= 4) {
     // ------------------------------------------- softmax + epilogue (x2) --
@@ -347,6 +364,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           a[64 + i] = __uint_as_float(r2[i]);
         }
       }
+      // The scores are in registers: S_t may take the next tile's scores.
+      tc_fence_before();
+      mbar_arrive(&bars.s_free[t]);
       if constexpr (kDumpS) {
         if (row_valid) {
           int32_t* drow = p.s_dump + (static_cast<size_t>(bh) * p.S + qrow) * p.S + j * kKV;
@@ -356,33 +376,37 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
 
       const int valid = p.S - j * kKV;    // keys of this tile that exist (>= 1)
+      if (valid < kKV) {
+#pragma unroll
+        for (int c = 0; c < kKV; ++c) a[c] = c < valid ? a[c] : -INFINITY;
+      }
       float mt = -INFINITY;
-      if (valid >= kKV) {
 #pragma unroll
-        for (int i = 0; i < 3; ++i) {
-          float mx = a[32 * i];
+      for (int i = 0; i < 3; ++i) {
+        float mx = a[32 * i];
 #pragma unroll
-          for (int c = 1; c < 31; c += 2) mx = fmax3(mx, a[32 * i + c], a[32 * i + c + 1]);
-          mx = fmaxf(mx, a[32 * i + 31]);
-          mt = fmaxf(mt, mx * cb[i]);
-        }
-      } else {
-#pragma unroll
-        for (int i = 0; i < 3; ++i) {
-          float mx = -INFINITY;
-#pragma unroll
-          for (int c = 0; c < 32; ++c) mx = (32 * i + c < valid) ? fmaxf(mx, a[32 * i + c]) : mx;
-          if (32 * i < valid) mt = fmaxf(mt, mx * cb[i]);
-        }
+        for (int c = 1; c < 31; c += 2) mx = fmax3(mx, a[32 * i + c], a[32 * i + c + 1]);
+        mx = fmaxf(mx, a[32 * i + 31]);
+        mt = fmaxf(mt, mx * cb[i]);       // a block past the end gives -inf or NaN: ignored
       }
       const float m_new = fmaxf(m_run, mt);
       const float bias = m_new - kLog2P;
-      if (valid >= kKV)
-        softmax_p<false>(a, cb, bias, valid, tS);
-      else
-        softmax_p<true>(a, cb, bias, valid, tS);
-      // Rescale O and L when the running max moved.  O is final here: this
-      // tile's scores were computed after the previous PV of this Q tile.
+      uint32_t pk[kKV / 4];
+      softmax_p(a, cb, bias, pk);
+      if (valid < kKV) {                  // keys past the end: code 0
+#pragma unroll
+        for (int w = 0; w < kKV / 4; ++w) {
+          const int keep = min(max(valid - 4 * w, 0), 4);
+          pk[w] &= keep == 4 ? 0xFFFFFFFFu : ((1u << (8 * keep)) - 1u);
+        }
+      }
+      // PV(j-1) of this tile has read the P~ buffer and left O final.
+      if (j > 0 && !__all_sync(0xFFFFFFFFu, wait_bar(&bars.pv_done[t], (j - 1) & 1, abort_v, p.timeout_ns))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      // Rescale O and L when the running max moved.
       const bool need = (j > 0) && (m_new != m_run);
       if (__any_sync(0xFFFFFFFFu, need)) {
         const float alpha = ex2_approx(m_run - m_new);
@@ -404,9 +428,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld_wait();
         l4[0] = __float_as_uint(__uint_as_float(l4[0]) * alpha);
         tmem_st4(tO + 128, l4);
+        tmem_st_wait();
       }
       m_run = m_new;
-      tmem_st_wait();
+      store_p_row(sP + t * kPTileBytes, row, pk);
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // P~ visible to the MMA
       tc_fence_before();
       mbar_arrive(&bars.p_full[t]);
     }

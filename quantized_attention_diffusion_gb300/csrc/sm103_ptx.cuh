@@ -61,13 +61,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Wait for the phase with the given parity to complete.  Returns false (and
-// leaves the block's abort flag set) if the block was aborted or the wait
-// ran past timeout_ns.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                          int* err_word, uint64_t timeout_ns) {
-  const uint32_t a = smem_addr(bar);
-  if (mbar_try_wait(a, parity)) return true;
+// Slow path of mbar_wait: poll until the phase completes, the block aborts
+// or timeout_ns of %globaltimer time pass.  Kept out of line so that the hot
+// loops that wait on barriers stay small in the instruction cache.
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t a, uint32_t parity, volatile int* abort_flag,
+                                            int* err_word, uint64_t timeout_ns) {
   const uint64_t t0 = global_timer_ns();
   while (true) {
 #pragma unroll 1
@@ -80,6 +78,16 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
       return false;
     }
   }
+}
+
+// Wait for the phase with the given parity to complete.  Returns false (and
+// leaves the block's abort flag set) if the block was aborted or the wait
+// ran past timeout_ns.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          int* err_word, uint64_t timeout_ns) {
+  const uint32_t a = smem_addr(bar);
+  if (mbar_try_wait(a, parity)) return true;
+  return mbar_wait_slow(a, parity, abort_flag, err_word, timeout_ns);
 }
 
 // ------------------------------------------------------------------ TMA --
@@ -100,21 +108,14 @@ __device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* m
 
 // --------------------------------------------------------------- tcgen05 --
 
-// Shared-memory matrix descriptor for a K-major operand laid out by TMA with
-// 128-byte swizzling: rows of 128 bytes, 8-row groups 1024 bytes apart.
+// Shared-memory matrix descriptors describe a K-major operand laid out by
+// TMA with 128-byte swizzling: rows of 128 bytes, 8-row groups 1024 bytes
+// apart.
 //   bits  0-13 start address >> 4
 //   bits 16-29 leading-dimension byte offset >> 4 (unused for this layout)
 //   bits 32-45 stride-dimension byte offset >> 4 (1024 B between 8-row groups)
 //   bits 46-47 descriptor version (1 on sm_100 family)
 //   bits 61-63 swizzle mode (2 = 128-byte swizzle)
-__device__ __forceinline__ uint64_t make_sw128_desc(uint32_t smem_byte_addr) {
-  uint64_t d = 0;
-  d |= static_cast<uint64_t>((smem_byte_addr & 0x3FFFFu) >> 4);
-  d |= static_cast<uint64_t>(1024u >> 4) << 32;
-  d |= static_cast<uint64_t>(1u) << 46;
-  d |= static_cast<uint64_t>(2u) << 61;
-  return d;
-}
 
 // Instruction descriptor for kind::f16 / kind::f8f6f4 with an FP32
 // accumulator, both operands K-major, no negation or sparsity.
@@ -147,23 +148,35 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D[tmem] (+)= A[smem] * B[smem]^T, kind::f16 (one K=16 step).
-__device__ __forceinline__ void mma_f16_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                           uint32_t idesc, uint32_t accumulate) {
+// Upper word of every shared-memory descriptor built here (SBO 1024 bytes,
+// version 1, 128-byte swizzle); the lower word is the start address >> 4.
+// Issuing threads keep only lower words and add constant offsets to them,
+// which keeps the MMA issue loops short.
+constexpr uint32_t kSw128DescHi = (1024u >> 4) | (1u << 14) | (2u << 29);
+__device__ __forceinline__ uint32_t sw128_desc_lo(uint32_t smem_byte_addr) {
+  return (smem_byte_addr & 0x3FFFFu) >> 4;
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T, kind::f16 (one K=16 step); A and B given
+// by the lower words of their descriptors.
+__device__ __forceinline__ void mma_f16_ss(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t idesc,
+                                           uint32_t accumulate) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "mov.b64 da, {%1, %5};\n\tmov.b64 db, {%2, %5};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_lo), "r"(b_lo), "r"(idesc), "r"(accumulate), "r"(kSw128DescHi)
       : "memory");
 }
 
-// D[tmem] (+)= A[tmem] * B[smem]^T, kind::f8f6f4 (one K=32 step).
-__device__ __forceinline__ void mma_f8_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                          uint32_t idesc, uint32_t accumulate) {
+// D[tmem] (+)= A[smem] * B[smem]^T, kind::f8f6f4 (one K=32 step).
+__device__ __forceinline__ void mma_f8_ss(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t idesc,
+                                          uint32_t accumulate) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "mov.b64 da, {%1, %5};\n\tmov.b64 db, {%2, %5};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], da, db, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_lo), "r"(b_lo), "r"(idesc), "r"(accumulate), "r"(kSw128DescHi)
       : "memory");
 }
 
