@@ -138,6 +138,22 @@ sage_status sage_attn_fwd_ws(const void* q, const void* k, const void* v, void* 
                              size_t workspace_bytes, void* stream);
 
 /*
+ * sage_attn_fwd_lse -- sage_attn_fwd that also writes each query row's
+ * log-sum-exp.  Passage: PR #15060, "What does this PR do?" (the pages' kernel
+ * returns no LSE; the LSE is what merging partial attentions of one query,
+ * e.g. over sequence shards, needs).
+ *
+ *   lse  out: fp32 [B, H, S] (device, 16-byte aligned), row (b, h, i) =
+ *             ln 2 * (m + log2 L - log2 448): m the row's final running max
+ *             of the base-2 scores, L its accumulated E4M3 weights (the
+ *             normaliser of `out`).  This is log sum_j exp(scale q_i . k_j)
+ *             as the quantised computation estimates it.
+ * Everything else, including errors, as sage_attn_fwd; `out` is identical.
+ */
+sage_status sage_attn_fwd_lse(const void* q, const void* k, const void* v, void* out, float* lse, int B,
+                              int S, int H, int D, float softmax_scale, void* stream);
+
+/*
  * sage_attn_fwd_quantized -- the attention step alone, from operands in the
  * layouts sage_quantize_qkv() writes (same passage as sage_attn_fwd).
  * `workspace` (caller-owned, >= sage_workspace_bytes) receives fp16 copies of

@@ -25,7 +25,7 @@ import threading
 
 import numpy as np
 
-from .fp64_reference import attention_fp64  # noqa: F401
+from .fp64_reference import attention_fp64, lse_fp64  # noqa: F401
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "sage_oracle.c")
@@ -70,7 +70,7 @@ def _load():
         lib.oracle_qk_int32.argtypes = [P, P, I, I, I, I, I, P]
         lib.oracle_attend_rows.restype = I
         lib.oracle_attend_rows.argtypes = [P, P, P, P, P, P, I, I, I, I, I,
-                                           ctypes.c_float, I, P, ctypes.c_int64, P, P]
+                                           ctypes.c_float, I, P, ctypes.c_int64, P, P, P, P]
         lib.oracle_attend_row_debug.restype = I
         lib.oracle_attend_row_debug.argtypes = [P, P, P, P, P, P, I, I, I, I, I,
                                                 ctypes.c_float, I, I, I, I, P, P, P, P]
@@ -156,27 +156,36 @@ def all_rows(B: int, S: int, H: int) -> np.ndarray:
 
 
 def attend_rows(quant, S: int, softmax_scale: float, rows: np.ndarray, l_mode: int = 0,
-                return_ties: bool = False):
+                return_ties: bool = False, return_lse: bool = False):
     """Attention output for selected query rows from quantised operands.
 
     quant = (q_codes, q_scale, k_codes, k_scale, vt_codes, v_scale) in the
     layouts returned by ``quantize_qk`` / ``quantize_v``.  rows: int32 [n, 3]
     of (b, h, i).  Returns bf16 bits [n, D]; with return_ties also each row's
     tie bound (float64 [n]): the most an equally correct rounding of P codes
-    that sit on an E4M3 rounding midpoint could move that row's outputs.
+    that sit on an E4M3 rounding midpoint could move that row's outputs; with
+    return_lse also each row's log-sum-exp (reading R13) and its tie bound
+    (two float64 [n]), appended in that order.
     """
     qc, qs, kc, ks, vt, vs = [np.ascontiguousarray(a) for a in quant]
     B, H, Sp, D = qc.shape
     rows = np.ascontiguousarray(rows, dtype=np.int32).reshape(-1, 3)
     out = np.empty((rows.shape[0], D), dtype=np.uint16)
     ties = np.zeros(rows.shape[0], dtype=np.float64)
+    lse = np.zeros(rows.shape[0], dtype=np.float64)
+    lse_ties = np.zeros(rows.shape[0], dtype=np.float64)
     rc = _load().oracle_attend_rows(_ptr(qc), _ptr(qs), _ptr(kc), _ptr(ks), _ptr(vt),
                                     _ptr(vs), B, S, H, D, Sp, float(softmax_scale),
                                     int(l_mode), _ptr(rows), rows.shape[0], _ptr(out),
-                                    _ptr(ties))
+                                    _ptr(ties), _ptr(lse), _ptr(lse_ties))
     if rc != 0:
         raise MemoryError("oracle_attend_rows failed to allocate")
-    return (out, ties) if return_ties else out
+    res = (out,)
+    if return_ties:
+        res += (ties,)
+    if return_lse:
+        res += (lse, lse_ties)
+    return res if len(res) > 1 else out
 
 
 def attend_row_debug(quant, S: int, softmax_scale: float, b: int, h: int, i: int,

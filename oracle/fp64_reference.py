@@ -56,3 +56,21 @@ def _attend(qh: np.ndarray, kh: np.ndarray, vh: np.ndarray, scale: float) -> np.
     p = np.exp(s)
     p /= p.sum(axis=1, keepdims=True)
     return p @ vh
+
+
+def lse_fp64(q: np.ndarray, k: np.ndarray, softmax_scale: float,
+             rows: np.ndarray) -> np.ndarray:
+    """float64 log-sum-exp of the scaled scores, ``log sum_j exp(scale q_i.k_j)``.
+
+    q, k: bf16 bits [B, S, H, D]; rows int [n, 3] of (b, h, i).  Returns
+    float64 [n].  The max is subtracted before exponentiating.
+    """
+    rows = np.asarray(rows).reshape(-1, 3)
+    out = np.empty(rows.shape[0], dtype=np.float64)
+    for n, (b, h, i) in enumerate(rows):
+        qi = bf16_bits_to_f64(q[int(b), int(i), int(h), :])
+        kh = bf16_bits_to_f64(k[int(b), :, int(h), :])
+        s = (kh @ qi) * softmax_scale
+        m = s.max()
+        out[n] = m + np.log(np.exp(s - m).sum())
+    return out

@@ -50,6 +50,11 @@
  *      double.  Within a tile every product is a multiple of 2^-18 below
  *      2^18, so each tile's sum is exact and independent of key order.
  *  R11 out[d] = bf16_rne((float)(O[d] * sv[d] / L)), layout [B, S, H, D].
+ *  R13 (LSE, optional output) lse = ln 2 * (m + log2 L - log2 448) in double,
+ *      with m the final running max (fp32, base 2) and L the normaliser of R9:
+ *      the natural log of sum_j exp(scores) as this quantised computation
+ *      estimates it (p_j = 448 * 2^(x_j - m), so sum_j 2^(x_j) ~ 2^m L / 448).
+ *      Tie bound for lse: ln(L / (L - T)).
  *
  *  Tie bound.  A P code whose p_j lies within 2^-19 (relative) of a
  *  rounding midpoint of the E4M3 grid is a tie: an implementation whose 2^x
@@ -248,7 +253,8 @@ static void attend_row(const int8_t *q, const float *qs, const int8_t *k,
                        int b, int h, int i, int S, int H, int D, int S_pad,
                        float softmax_scale, int l_mode, float *sbuf,
                        int32_t *acc, uint8_t *cbuf, double *obuf, uint16_t *out_row,
-                       uint8_t *pcodes, double *L_out, double *tie_out) {
+                       uint8_t *pcodes, double *L_out, double *tie_out,
+                       double *lse_out, double *lse_tie_out) {
     int nb = (S + 31) / 32;
     const int8_t *qi = q + (((size_t)b * H + h) * S_pad + i) * D;
     const float *vsh = vs + ((size_t)b * H + h) * D;
@@ -302,6 +308,9 @@ static void attend_row(const int8_t *q, const float *qs, const int8_t *k,
     if (pcodes) memcpy(pcodes, cbuf, (size_t)S);
     if (L_out) *L_out = L;
     if (tie_out) *tie_out = (T > 0.0 && L > T) ? T * 2.0 * vmax / (L - T) : (T > 0.0 ? INFINITY : 0.0);
+    /* R13 */
+    if (lse_out) *lse_out = log(2.0) * ((double)m_run + log2(L) - log2(448.0));
+    if (lse_tie_out) *lse_tie_out = (T > 0.0 && L > T) ? log(L / (L - T)) : (T > 0.0 ? INFINITY : 0.0);
 }
 
 /* Decode one head's V^T codes into [S][D] floats (e4m3 values are exact in
@@ -317,14 +326,16 @@ static void decode_v_head(const uint8_t *vt, int b, int h, int S, int H, int D,
 /* Attention output for a list of query rows.  rows: n triples (b, h, i).
  * out: bf16 [n, D] in the order of rows.  Every (b, h) named in rows must
  * appear; heads are decoded once.  ties (may be NULL): double [n], each
- * row's tie bound.  Returns 0, or -1 on allocation failure.
- * [I15014] bullets 1-2, [P15060] ("no LSE"): the output is the normalised
- * attention only. */
+ * row's tie bound.  lse, lse_ties (may be NULL): double [n], each row's
+ * log-sum-exp (R13) and its tie bound.  Returns 0, or -1 on allocation
+ * failure.  [I15014] bullets 1-2, [P15060] ("no LSE"): the kernel contract's
+ * output is the normalised attention; the LSE is the optional extra output. */
 int oracle_attend_rows(const int8_t *q, const float *qs, const int8_t *k,
                        const float *ks, const uint8_t *vt, const float *vs,
                        int B, int S, int H, int D, int S_pad,
                        float softmax_scale, int l_mode, const int32_t *rows,
-                       int64_t n, uint16_t *out, double *ties) {
+                       int64_t n, uint16_t *out, double *ties, double *lse,
+                       double *lse_ties) {
     /* decode the heads in use */
     int nheads = B * H;
     float **vdec = (float **)calloc((size_t)nheads, sizeof(float *));
@@ -356,7 +367,8 @@ int oracle_attend_rows(const int8_t *q, const float *qs, const int8_t *k,
                     int b = rows[3 * r], h = rows[3 * r + 1], i = rows[3 * r + 2];
                     attend_row(q, qs, k, ks, vdec[b * H + h], vs, b, h, i, S, H, D,
                                S_pad, softmax_scale, l_mode, sbuf, abuf, cbuf, obuf,
-                               out + (size_t)r * D, NULL, NULL, ties ? ties + r : NULL);
+                               out + (size_t)r * D, NULL, NULL, ties ? ties + r : NULL,
+                               lse ? lse + r : NULL, lse_ties ? lse_ties + r : NULL);
                 }
             }
             free(sbuf); free(abuf); free(cbuf); free(obuf);
@@ -385,7 +397,7 @@ int oracle_attend_row_debug(const int8_t *q, const float *qs, const int8_t *k,
     if (vdec && sbuf && abuf && cbuf && obuf) {
         decode_v_head(vt, b, h, S, H, D, S_pad, vdec);
         attend_row(q, qs, k, ks, vdec, vs, b, h, i, S, H, D, S_pad, softmax_scale,
-                   l_mode, sbuf, abuf, cbuf, obuf, out_row, pcodes, L_out, tie_out);
+                   l_mode, sbuf, abuf, cbuf, obuf, out_row, pcodes, L_out, tie_out, NULL, NULL);
         rc = 0;
     }
     free(vdec); free(sbuf); free(abuf); free(cbuf); free(obuf);

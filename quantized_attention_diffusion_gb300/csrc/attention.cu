@@ -83,6 +83,7 @@ __host__ __device__ constexpr uint32_t col_s(int t) { return static_cast<uint32_
 __host__ __device__ constexpr uint32_t col_o(int t) { return 2 * kKV + static_cast<uint32_t>(t) * 144; }
 constexpr float kLog2P = 8.80735492706298828125f;         // fp32(log2 448): P scale 448
 constexpr float kLog2e = 1.44269502162933349609375f;      // fp32(log2 e)
+constexpr float kLn2 = 0.693147182464599609375f;          // fp32(ln 2)
 constexpr uint32_t kE4M3One = 0x38383838u;                // four E4M3 1.0
 
 static_assert(kSmemDynamic <= 227 * 1024 - 1024, "shared memory budget");
@@ -93,6 +94,7 @@ struct Params {
   const float* v_scale;
   uint16_t* out;
   int32_t* s_dump;
+  float* lse;             // optional [B, H, S]
   int S, H, S_pad, nb, n_kv, n_pairs;
   float c_scale;          // fp32(softmax_scale * fp32(log2 e))
   uint64_t timeout_ns;
@@ -444,6 +446,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld4(tO + 128, l4);
       tmem_ld_wait();
       const float inv_l = 1.0f / __uint_as_float(l4[0]);
+      // log sum_j exp(score_j) = ln 2 * (m + log2 L - log2 448): P~ = 448 at the max.
+      if (p.lse != nullptr && row_valid)
+        p.lse[static_cast<size_t>(bh) * p.S + qrow] = (m_run + log2f(__uint_as_float(l4[0])) - kLog2P) * kLn2;
       const int b = bh / p.H, h = bh % p.H;
       uint16_t* orow = p.out + ((static_cast<size_t>(b) * p.S + qrow) * p.H + h) * kHeadDim;
 #pragma unroll
@@ -532,6 +537,7 @@ cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream) {
   p.v_scale = a.v_scale;
   p.out = a.out;
   p.s_dump = a.s_dump;
+  p.lse = a.lse;
   p.S = a.S;
   p.H = a.H;
   p.S_pad = a.S_pad;

@@ -122,7 +122,7 @@ cudaError_t pool_alloc(void** ptr, size_t bytes, cudaStream_t stream) {
 uint64_t timeout_ns() { return g_timeout_ns.load(std::memory_order_relaxed); }
 
 sage_status run_fused(const void* q, const void* k, const void* v, void* out, int B, int S, int H,
-                      float softmax_scale, void* ws, cudaStream_t st) {
+                      float softmax_scale, void* ws, cudaStream_t st, float* lse = nullptr) {
   const WsLayout w = ws_layout(B, S, H);
   const int Sp = padded_len(S), nb = num_blocks(S);
   QKQuantArgs<__half> qa;
@@ -151,6 +151,7 @@ sage_status run_fused(const void* q, const void* k, const void* v, void* out, in
   aa.v_scale = at<float>(ws, w.vs);
   aa.out = static_cast<uint16_t*>(out);
   aa.s_dump = nullptr;
+  aa.lse = lse;
   aa.B = B;
   aa.S = S;
   aa.H = H;
@@ -186,6 +187,7 @@ sage_status run_quantized(const int8_t* q_i8, const float* q_scale, const int8_t
   aa.v_scale = v_scale;
   aa.out = static_cast<uint16_t*>(out);
   aa.s_dump = s_dump;
+  aa.lse = nullptr;
   aa.B = B;
   aa.S = S;
   aa.H = H;
@@ -287,6 +289,25 @@ sage_status sage_attn_fwd(const void* q, const void* k, const void* v, void* out
     return fail(SAGE_ERR_NO_MEMORY, "workspace allocation of %zu bytes failed: %s", ws_layout(B, S, H).total,
                 cudaGetErrorString(e));
   s = run_fused(q, k, v, out, B, S, H, softmax_scale, ws, st);
+  e = cudaFreeAsync(ws, st);
+  if (s != SAGE_OK) return s;
+  if (e != cudaSuccess) return cuda_fail(e, "workspace release");
+  return SAGE_OK;
+}
+
+sage_status sage_attn_fwd_lse(const void* q, const void* k, const void* v, void* out, float* lse, int B,
+                              int S, int H, int D, float softmax_scale, void* stream) {
+  sage_status s = check_shape(B, S, H, D);
+  if (s == SAGE_OK) s = check_scale(softmax_scale);
+  if (s == SAGE_OK) s = check_ptrs({{q, "q"}, {k, "k"}, {v, "v"}, {out, "out"}, {lse, "lse"}});
+  if (s != SAGE_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  void* ws = nullptr;
+  cudaError_t e = pool_alloc(&ws, ws_layout(B, S, H).total, st);
+  if (e != cudaSuccess)
+    return fail(SAGE_ERR_NO_MEMORY, "workspace allocation of %zu bytes failed: %s", ws_layout(B, S, H).total,
+                cudaGetErrorString(e));
+  s = run_fused(q, k, v, out, B, S, H, softmax_scale, ws, st, lse);
   e = cudaFreeAsync(ws, st);
   if (s != SAGE_OK) return s;
   if (e != cudaSuccess) return cuda_fail(e, "workspace release");

@@ -49,6 +49,7 @@ struct AttnArgs {
   const float* v_scale;     // [B, H, 128]
   uint16_t* out;            // bf16 [B, S, H, 128]
   int32_t* s_dump;          // optional int32 Q K^T [B, H, S, S] (debug entry only)
+  float* lse;               // optional fp32 [B, H, S]: per-row log-sum-exp
   int B, S, H, S_pad, nb;
   float softmax_scale;
   uint64_t timeout_ns;

@@ -33,7 +33,7 @@ EXPORTED = (
     "sage_attn_fwd_ws", "sage_attn_fwd_quantized", "sage_debug_qk_int32",
     "sage_debug_wait_timeout", "sage_sync_status", "sage_set_wait_timeout_ns",
     "sage_last_error", "sage_status_string", "sage_set_attention_events",
-    "sage_quantize_qkv_noalloc",
+    "sage_quantize_qkv_noalloc", "sage_attn_fwd_lse",
 )
 
 
@@ -69,6 +69,7 @@ def load_library(path: str = LIB_PATH):
             "sage_quantize_qkv_noalloc": (S, [P, P, P, I, I, I, I, P, P, P, P, P, P, P]),
             "sage_attn_fwd": (S, [P, P, P, P, I, I, I, I, F, P]),
             "sage_attn_fwd_ws": (S, [P, P, P, P, I, I, I, I, F, P, Z, P]),
+            "sage_attn_fwd_lse": (S, [P, P, P, P, P, I, I, I, I, F, P]),
             "sage_attn_fwd_quantized": (S, [P, P, P, P, P, P, P, I, I, I, I, F, P, Z, P]),
             "sage_debug_qk_int32": (S, [P, P, P, P, P, P, P, P, I, I, I, I, F, P, Z, P]),
             "sage_debug_wait_timeout": (S, [ctypes.c_uint64, P]),
@@ -151,6 +152,29 @@ def attn_fwd(q, k, v, softmax_scale: float | None = None, out=None, workspace=No
                                         float(softmax_scale), _ptr(workspace),
                                         workspace.numel() * workspace.element_size(), st))
     return out
+
+
+def attn_fwd_lse(q, k, v, softmax_scale: float | None = None, out=None, lse=None):
+    """attn_fwd that also returns each query row's log-sum-exp.
+
+    Returns (out bf16 [B, S, H, 128], lse fp32 [B, H, S]); ``out`` and
+    ``lse`` may be given to be filled (sage_attn_fwd_lse).
+    """
+    lib = load_library()
+    B, S, H, D = _check_qkv(q, k, v)
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, S), dtype=torch.float32, device=q.device)
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, S) or not lse.is_contiguous() \
+            or lse.device != q.device:
+        raise ValueError("lse must be a contiguous float32 [B, H, S] tensor on q's device")
+    with torch.cuda.device(q.device):
+        _check(lib.sage_attn_fwd_lse(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, S, H, D,
+                                     float(softmax_scale), _stream(q.device)))
+    return out, lse
 
 
 def quantize_qkv(q, k, v, out=None, noalloc=False):

@@ -80,3 +80,17 @@ def assert_close_to_oracle(got, ref, ties, what=""):
         raise AssertionError(f"{what}: {int(bad.sum())} outputs beyond tolerance; worst at {i}: "
                              f"gpu {got[i]} oracle {ref[i]} tol {tol[i]:.4g}")
     return float(err.max()), int((np.asarray(ties) > 0).sum())
+
+
+def lse_tolerance(S, lse_ref, lse_ties):
+    """Per-row bound on |lse_gpu - lse_oracle| (same codes and running max on
+    both sides; see the derivation in the design notes): the kernel's fp32
+    row sum L is accumulated by the tensor cores over S/32 E4M3 MMA steps and
+    rescaled at most S/96 times, each a relative rounding of at most 2^-24;
+    the final fp32 expression (m + log2f(L) - log2 448) * ln 2 adds a few
+    roundings of a value below |m| + 32 (|m| <= |lse|/ln 2 + log2 S); plus
+    the oracle's LSE tie bound."""
+    eps = 2.0 ** -24
+    steps = S / 32 + S / 96 + 4
+    mag = np.abs(np.asarray(lse_ref)) / math.log(2) + math.log2(max(S, 1)) + 32
+    return steps * eps + 8 * eps * mag + np.asarray(lse_ties)
