@@ -51,6 +51,8 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="approximate CPU time budget of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--lse", action="store_true",
+                    help="time sage_attn_fwd_lse (also writes the per-row log-sum-exp)")
     ap.add_argument("--no-e2e", action="store_true",
                     help="skip the host-buffer leg (for short profiling runs; the line then has no e2e figure)")
     return ap.parse_args()
@@ -243,10 +245,17 @@ def run_ours(args, group, local):
     q, k, v = (t.to(dev) for t in (q_h, k_h, v_h))
     cpu_sample = [t[:1, :, :1].clone() for t in (q_h, k_h, v_h)]   # one (b, h) for the oracle leg
     out = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.S), dtype=torch.float32, device=dev) if args.lse else None
     K, W = args.steps, args.warmup
 
+    def step(qq, kk, vv, oo, ll=None):
+        if args.lse:
+            qad.attn_fwd_lse(qq, kk, vv, w.softmax_scale, out=oo, lse=ll)
+        else:
+            qad.attn_fwd(qq, kk, vv, w.softmax_scale, out=oo)
+
     for _ in range(W):
-        qad.attn_fwd(q, k, v, w.softmax_scale, out=out)
+        step(q, k, v, out, lse)
     torch.cuda.synchronize()
 
     # per-step events around the attention kernel (materialise handles first)
@@ -265,7 +274,7 @@ def run_ours(args, group, local):
     start.record()
     for i in range(K):
         qad.set_attention_events(before[i], after[i])
-        qad.attn_fwd(q, k, v, w.softmax_scale, out=out)
+        step(q, k, v, out, lse)
     end.record()
     torch.cuda.synchronize()
     qad.set_attention_events()
@@ -278,7 +287,7 @@ def run_ours(args, group, local):
     value = group.world * w.ops * K / (ms_max * 1e-3) / 1e12
 
     # End to end through the public API with host buffers: every step copies
-    # its Q/K/V from pinned host memory to the device, runs sage_attn_fwd and
+    # its Q/K/V from pinned host memory to the device, runs the step and
     # copies its output back to pinned host memory.  Device buffers are
     # double-buffered and the copies run on their own streams, so step i+1's
     # upload and step i-1's download overlap step i's compute, as a serving
@@ -288,9 +297,11 @@ def run_ours(args, group, local):
     if not args.no_e2e:
         host_in = [t.pin_memory() for t in (q_h, k_h, v_h)]
         host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        host_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory() if args.lse else None
         del q_h, k_h, v_h
         bufs = [[torch.empty_like(q) for _ in range(3)] for _ in range(2)]
         outs = [torch.empty_like(out) for _ in range(2)]
+        lses = [torch.empty_like(lse) for _ in range(2)] if args.lse else [None, None]
         comp = torch.cuda.current_stream(dev)
         up, down = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
 
@@ -311,11 +322,13 @@ def run_ours(args, group, local):
                     comp.wait_event(h2d[i - 1])
                     if i - 1 >= 2:
                         comp.wait_event(d2h[i - 3])             # output buffer b was read back
-                    qad.attn_fwd(*bufs[b], w.softmax_scale, out=outs[b])
+                    step(*bufs[b], outs[b], lses[b])
                     done[i - 1].record(comp)
                     with torch.cuda.stream(down):
                         down.wait_event(done[i - 1])
                         host_out.copy_(outs[b], non_blocking=True)
+                        if args.lse:
+                            host_lse.copy_(lses[b], non_blocking=True)
                         d2h[i - 1].record(down)
             comp.wait_event(d2h[n - 1])
 
@@ -332,7 +345,7 @@ def run_ours(args, group, local):
         e2e_ms = group.max(s2.elapsed_time(e2))
         e2e_value = group.world * w.ops * K2 / (e2e_ms * 1e-3) / 1e12
     in_bytes = 3 * q.numel() * q.element_size()
-    out_bytes = out.numel() * out.element_size()
+    out_bytes = out.numel() * out.element_size() + (lse.numel() * 4 if args.lse else 0)
 
     peak, p_bf16, hbm, src, peak_burst = tensor_peak()
     achieved = w.ops / (attn_ms_max * 1e-3) / 1e12
@@ -351,7 +364,8 @@ def run_ours(args, group, local):
         "data": "synthetic (seeded; shapes and distributions of the pages' diffusion workloads)",
         "config": {
             "workload": w.name, "B": w.B, "S": w.S, "H": w.H, "D": w.D, "recipe": w.recipe,
-            "seed": w.seed, "softmax_scale": w.softmax_scale, "path": "sage_attn_fwd (quantise + attention)",
+            "seed": w.seed, "softmax_scale": w.softmax_scale, "path": "sage_attn_fwd_lse (quantise + attention + LSE)" if args.lse
+            else "sage_attn_fwd (quantise + attention)",
             "l2": f"inputs larger than L2 ({in_bytes / 1e6:.0f} MB read per step, L2 129 MB)",
             "parallelism": "replicas" if group.world > 1 else "single GPU",
         },

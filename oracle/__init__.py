@@ -71,6 +71,9 @@ def _load():
         lib.oracle_attend_rows.restype = I
         lib.oracle_attend_rows.argtypes = [P, P, P, P, P, P, I, I, I, I, I,
                                            ctypes.c_float, I, P, ctypes.c_int64, P, P, P, P]
+        lib.oracle_attend_rows_cross.restype = I
+        lib.oracle_attend_rows_cross.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, I,
+                                                 ctypes.c_float, I, P, ctypes.c_int64, P, P, P, P]
         lib.oracle_attend_row_debug.restype = I
         lib.oracle_attend_row_debug.argtypes = [P, P, P, P, P, P, I, I, I, I, I,
                                                 ctypes.c_float, I, I, I, I, P, P, P, P]
@@ -156,7 +159,7 @@ def all_rows(B: int, S: int, H: int) -> np.ndarray:
 
 
 def attend_rows(quant, S: int, softmax_scale: float, rows: np.ndarray, l_mode: int = 0,
-                return_ties: bool = False, return_lse: bool = False):
+                return_ties: bool = False, return_lse: bool = False, Skv: int | None = None):
     """Attention output for selected query rows from quantised operands.
 
     quant = (q_codes, q_scale, k_codes, k_scale, vt_codes, v_scale) in the
@@ -165,19 +168,24 @@ def attend_rows(quant, S: int, softmax_scale: float, rows: np.ndarray, l_mode: i
     tie bound (float64 [n]): the most an equally correct rounding of P codes
     that sit on an E4M3 rounding midpoint could move that row's outputs; with
     return_lse also each row's log-sum-exp (reading R13) and its tie bound
-    (two float64 [n]), appended in that order.
+    (two float64 [n]), appended in that order.  S is the number of query
+    rows; Skv (default S) the number of keys and values (cross-attention,
+    reading R14).
     """
     qc, qs, kc, ks, vt, vs = [np.ascontiguousarray(a) for a in quant]
     B, H, Sp, D = qc.shape
+    Skv = S if Skv is None else int(Skv)
+    Skv_pad = kc.shape[2]
     rows = np.ascontiguousarray(rows, dtype=np.int32).reshape(-1, 3)
     out = np.empty((rows.shape[0], D), dtype=np.uint16)
     ties = np.zeros(rows.shape[0], dtype=np.float64)
     lse = np.zeros(rows.shape[0], dtype=np.float64)
     lse_ties = np.zeros(rows.shape[0], dtype=np.float64)
-    rc = _load().oracle_attend_rows(_ptr(qc), _ptr(qs), _ptr(kc), _ptr(ks), _ptr(vt),
-                                    _ptr(vs), B, S, H, D, Sp, float(softmax_scale),
-                                    int(l_mode), _ptr(rows), rows.shape[0], _ptr(out),
-                                    _ptr(ties), _ptr(lse), _ptr(lse_ties))
+    rc = _load().oracle_attend_rows_cross(_ptr(qc), _ptr(qs), _ptr(kc), _ptr(ks), _ptr(vt),
+                                          _ptr(vs), B, S, Skv, H, D, Sp, Skv_pad,
+                                          float(softmax_scale), int(l_mode), _ptr(rows),
+                                          rows.shape[0], _ptr(out), _ptr(ties), _ptr(lse),
+                                          _ptr(lse_ties))
     if rc != 0:
         raise MemoryError("oracle_attend_rows failed to allocate")
     res = (out,)
@@ -222,10 +230,11 @@ def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, softmax_scale: float,
     bf16 bits [n, D] (ties [n]) for the given (b, h, i) rows.
     """
     B, S, H, D = q.shape
+    Skv = k.shape[1]
     quant = quantize(q, k, v)
     if rows is None:
-        out, ties = attend_rows(quant, S, softmax_scale, all_rows(B, S, H), l_mode, True)
+        out, ties = attend_rows(quant, S, softmax_scale, all_rows(B, S, H), l_mode, True, Skv=Skv)
         out, ties = out.reshape(B, S, H, D), ties.reshape(B, S, H)
     else:
-        out, ties = attend_rows(quant, S, softmax_scale, rows, l_mode, True)
+        out, ties = attend_rows(quant, S, softmax_scale, rows, l_mode, True, Skv=Skv)
     return (out, ties) if return_ties else out

@@ -55,6 +55,9 @@
  *      the natural log of sum_j exp(scores) as this quantised computation
  *      estimates it (p_j = 448 * 2^(x_j - m), so sum_j 2^(x_j) ~ 2^m L / 448).
  *      Tie bound for lse: ln(L / (L - T)).
+ *  R14 (cross-attention) Q may have Sq rows and K, V S != Sq rows: each is
+ *      quantised over its own 32-row blocks (Q, K) or its own tokens (V);
+ *      every step above runs over the S keys unchanged.
  *
  *  Tie bound.  A P code whose p_j lies within 2^-19 (relative) of a
  *  rounding midpoint of the E4M3 grid is a tie: an implementation whose 2^x
@@ -243,22 +246,24 @@ static double tie_step(float y, uint8_t code) {
     return fabs(other - v);
 }
 
-/* One query row (b, h, i).  Writes D bf16 outputs to out_row.  If pcodes is
+/* One query row (b, h, i) of Q (Sq rows, padded to Sq_pad) against S keys
+ * and values (padded to S_pad): S = Sq for self-attention, S != Sq for
+ * cross-attention (reading R14).  Writes D bf16 outputs to out_row.  If pcodes is
  * not NULL it receives the S FP8 codes of P (each against the running max of
  * its tile) and *L_out the normaliser; *tie_out (if not NULL) the row's tie
  * bound.  vdec is this head's decoded V, [S][D] floats (exact); acc is
  * scratch for one tile's integer scores.  R6..R11. */
 static void attend_row(const int8_t *q, const float *qs, const int8_t *k,
                        const float *ks, const float *vdec, const float *vs,
-                       int b, int h, int i, int S, int H, int D, int S_pad,
+                       int b, int h, int i, int Sq, int S, int H, int D, int Sq_pad, int S_pad,
                        float softmax_scale, int l_mode, float *sbuf,
                        int32_t *acc, uint8_t *cbuf, double *obuf, uint16_t *out_row,
                        uint8_t *pcodes, double *L_out, double *tie_out,
                        double *lse_out, double *lse_tie_out) {
-    int nb = (S + 31) / 32;
-    const int8_t *qi = q + (((size_t)b * H + h) * S_pad + i) * D;
+    int nb = (S + 31) / 32, nbq = (Sq + 31) / 32;
+    const int8_t *qi = q + (((size_t)b * H + h) * Sq_pad + i) * D;
     const float *vsh = vs + ((size_t)b * H + h) * D;
-    float sq = qs[((size_t)b * H + h) * nb + i / 32];
+    float sq = qs[((size_t)b * H + h) * nbq + i / 32];
     float c = softmax_scale * ORACLE_L2E;
     float c_row = sq * c;
     double L = 0.0, T = 0.0;
@@ -330,12 +335,12 @@ static void decode_v_head(const uint8_t *vt, int b, int h, int S, int H, int D,
  * log-sum-exp (R13) and its tie bound.  Returns 0, or -1 on allocation
  * failure.  [I15014] bullets 1-2, [P15060] ("no LSE"): the kernel contract's
  * output is the normalised attention; the LSE is the optional extra output. */
-int oracle_attend_rows(const int8_t *q, const float *qs, const int8_t *k,
-                       const float *ks, const uint8_t *vt, const float *vs,
-                       int B, int S, int H, int D, int S_pad,
-                       float softmax_scale, int l_mode, const int32_t *rows,
-                       int64_t n, uint16_t *out, double *ties, double *lse,
-                       double *lse_ties) {
+int oracle_attend_rows_cross(const int8_t *q, const float *qs, const int8_t *k,
+                             const float *ks, const uint8_t *vt, const float *vs,
+                             int B, int Sq, int S, int H, int D, int Sq_pad, int S_pad,
+                             float softmax_scale, int l_mode, const int32_t *rows,
+                             int64_t n, uint16_t *out, double *ties, double *lse,
+                             double *lse_ties) {
     /* decode the heads in use */
     int nheads = B * H;
     float **vdec = (float **)calloc((size_t)nheads, sizeof(float *));
@@ -365,8 +370,8 @@ int oracle_attend_rows(const int8_t *q, const float *qs, const int8_t *k,
 #pragma omp for schedule(dynamic, 4)
                 for (int64_t r = 0; r < n; ++r) {
                     int b = rows[3 * r], h = rows[3 * r + 1], i = rows[3 * r + 2];
-                    attend_row(q, qs, k, ks, vdec[b * H + h], vs, b, h, i, S, H, D,
-                               S_pad, softmax_scale, l_mode, sbuf, abuf, cbuf, obuf,
+                    attend_row(q, qs, k, ks, vdec[b * H + h], vs, b, h, i, Sq, S, H, D,
+                               Sq_pad, S_pad, softmax_scale, l_mode, sbuf, abuf, cbuf, obuf,
                                out + (size_t)r * D, NULL, NULL, ties ? ties + r : NULL,
                                lse ? lse + r : NULL, lse_ties ? lse_ties + r : NULL);
                 }
@@ -377,6 +382,17 @@ int oracle_attend_rows(const int8_t *q, const float *qs, const int8_t *k,
     for (int bh = 0; bh < nheads; ++bh) free(vdec[bh]);
     free(vdec);
     return fail ? -1 : 0;
+}
+
+/* Self-attention: Q, K and V share the length S. */
+int oracle_attend_rows(const int8_t *q, const float *qs, const int8_t *k,
+                       const float *ks, const uint8_t *vt, const float *vs,
+                       int B, int S, int H, int D, int S_pad,
+                       float softmax_scale, int l_mode, const int32_t *rows,
+                       int64_t n, uint16_t *out, double *ties, double *lse,
+                       double *lse_ties) {
+    return oracle_attend_rows_cross(q, qs, k, ks, vt, vs, B, S, S, H, D, S_pad, S_pad,
+                                    softmax_scale, l_mode, rows, n, out, ties, lse, lse_ties);
 }
 
 /* Single row with its FP8 P codes and normaliser exposed (for the pins on
@@ -396,7 +412,7 @@ int oracle_attend_row_debug(const int8_t *q, const float *qs, const int8_t *k,
     int rc = -1;
     if (vdec && sbuf && abuf && cbuf && obuf) {
         decode_v_head(vt, b, h, S, H, D, S_pad, vdec);
-        attend_row(q, qs, k, ks, vdec, vs, b, h, i, S, H, D, S_pad, softmax_scale,
+        attend_row(q, qs, k, ks, vdec, vs, b, h, i, S, S, H, D, S_pad, S_pad, softmax_scale,
                    l_mode, sbuf, abuf, cbuf, obuf, out_row, pcodes, L_out, tie_out, NULL, NULL);
         rc = 0;
     }
