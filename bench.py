@@ -213,7 +213,7 @@ def oracle_sample(w, q, k, v, seconds: float, steps: int = 1):
         quant = oracle.quantize(*sl)
         rows = np.stack([np.zeros(n_rows), np.zeros(n_rows),
                          np.linspace(0, w.S - 1, n_rows).round()], axis=1).astype(np.int32)
-        oracle.attend_rows(quant, w.S, w.softmax_scale, rows)
+        oracle.attend_rows(quant, w.S, w.softmax_scale, rows, Skv=w.skv)
         return time.perf_counter() - t0
 
     n_cal = 64
@@ -223,9 +223,9 @@ def oracle_sample(w, q, k, v, seconds: float, steps: int = 1):
     n_rows = int(max(8, min(w.S, (seconds - t_quant) / per_row)))
     times = [run(n_rows) for _ in range(steps)]
     t = statistics.median(times) if steps > 1 else times[0]
-    ops = 4.0 * n_rows * w.S * w.D
-    sample = (f"one (b,h) of {w.name}: quantise its {w.S} tokens, then attention for {n_rows} "
-              f"of its query rows ({ops:.3g} ops)")
+    ops = 4.0 * n_rows * w.skv * w.D
+    sample = (f"one (b,h) of {w.name}: quantise its {w.S} query and {w.skv} key/value tokens, "
+              f"then attention for {n_rows} of its query rows ({ops:.3g} ops)")
     return ops / t / 1e12, sample, oracle.num_threads(), ops, times
 
 
@@ -249,7 +249,9 @@ def run_ours(args, group, local):
     K, W = args.steps, args.warmup
 
     def step(qq, kk, vv, oo, ll=None):
-        if args.lse:
+        if w.Skv is not None:
+            qad.attn_fwd_cross(qq, kk, vv, w.softmax_scale, out=oo, lse=ll)
+        elif args.lse:
             qad.attn_fwd_lse(qq, kk, vv, w.softmax_scale, out=oo, lse=ll)
         else:
             qad.attn_fwd(qq, kk, vv, w.softmax_scale, out=oo)
@@ -299,7 +301,7 @@ def run_ours(args, group, local):
         host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
         host_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory() if args.lse else None
         del q_h, k_h, v_h
-        bufs = [[torch.empty_like(q) for _ in range(3)] for _ in range(2)]
+        bufs = [[torch.empty_like(t) for t in (q, k, v)] for _ in range(2)]
         outs = [torch.empty_like(out) for _ in range(2)]
         lses = [torch.empty_like(lse) for _ in range(2)] if args.lse else [None, None]
         comp = torch.cuda.current_stream(dev)
@@ -344,7 +346,7 @@ def run_ours(args, group, local):
         group.barrier()
         e2e_ms = group.max(s2.elapsed_time(e2))
         e2e_value = group.world * w.ops * K2 / (e2e_ms * 1e-3) / 1e12
-    in_bytes = 3 * q.numel() * q.element_size()
+    in_bytes = (q.numel() + k.numel() + v.numel()) * q.element_size()
     out_bytes = out.numel() * out.element_size() + (lse.numel() * 4 if args.lse else 0)
 
     peak, p_bf16, hbm, src, peak_burst = tensor_peak()
@@ -363,9 +365,10 @@ def run_ours(args, group, local):
         "dtype": DTYPE,
         "data": "synthetic (seeded; shapes and distributions of the pages' diffusion workloads)",
         "config": {
-            "workload": w.name, "B": w.B, "S": w.S, "H": w.H, "D": w.D, "recipe": w.recipe,
-            "seed": w.seed, "softmax_scale": w.softmax_scale, "path": "sage_attn_fwd_lse (quantise + attention + LSE)" if args.lse
-            else "sage_attn_fwd (quantise + attention)",
+            "workload": w.name, "B": w.B, "S": w.S, "Skv": w.skv, "H": w.H, "D": w.D, "recipe": w.recipe,
+            "seed": w.seed, "softmax_scale": w.softmax_scale, "path": ("sage_attn_fwd_cross" if w.Skv is not None else "sage_attn_fwd_lse" if args.lse
+                     else "sage_attn_fwd") + (" (quantise + attention + LSE)" if args.lse
+                                               else " (quantise + attention)"),
             "l2": f"inputs larger than L2 ({in_bytes / 1e6:.0f} MB read per step, L2 129 MB)",
             "parallelism": "replicas" if group.world > 1 else "single GPU",
         },
@@ -410,7 +413,7 @@ def run_reference(args):
         "ms_per_step": round(t * 1e3, 3), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": DTYPE,
         "data": "synthetic (seeded; shapes and distributions of the pages' diffusion workloads)",
-        "config": {"workload": w.name, "B": w.B, "S": w.S, "H": w.H, "D": w.D, "recipe": w.recipe,
+        "config": {"workload": w.name, "B": w.B, "S": w.S, "Skv": w.skv, "H": w.H, "D": w.D, "recipe": w.recipe,
                    "seed": w.seed, "softmax_scale": w.softmax_scale,
                    "path": "CPU oracle (plain C, OpenMP) on a bounded sample per step"},
         "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": cores, "kind": "oracle",

@@ -154,6 +154,23 @@ sage_status sage_attn_fwd_lse(const void* q, const void* k, const void* v, void*
                               int S, int H, int D, float softmax_scale, void* stream);
 
 /*
+ * sage_attn_fwd_cross -- quantised cross-attention: Q has Sq rows, K and V
+ * have Skv rows (Skv != Sq allowed; Skv == Sq gives sage_attn_fwd exactly).
+ * Passage: the pages' second workload, shorter K/V, which the gfx1201 kernel
+ * sends to its fallback (issue #15014, "Describe the solution you'd like";
+ * SageAttention 2.2 results in InvokeAI PR #9657, "Summary").
+ *
+ *   q         in : bf16 [B, Sq, H, D]; k, v in: bf16 [B, Skv, H, D]
+ *   out       out: bf16 [B, Sq, H, D]
+ *   lse       out: fp32 [B, H, Sq] as sage_attn_fwd_lse, or NULL for none
+ * Q and K are quantised over their own 32-row blocks, V per channel over
+ * its own Skv tokens.  Shape limits (D = 128, lengths >= 1) apply to both
+ * lengths; errors as sage_attn_fwd.
+ */
+sage_status sage_attn_fwd_cross(const void* q, const void* k, const void* v, void* out, float* lse, int B,
+                                int Sq, int Skv, int H, int D, float softmax_scale, void* stream);
+
+/*
  * sage_attn_fwd_quantized -- the attention step alone, from operands in the
  * layouts sage_quantize_qkv() writes (same passage as sage_attn_fwd).
  * `workspace` (caller-owned, >= sage_workspace_bytes) receives fp16 copies of
@@ -197,7 +214,7 @@ sage_status sage_sync_status(void* stream);
 void sage_set_wait_timeout_ns(uint64_t ns);
 
 /* Timing hook (no counterpart on the pages): while set, every
- * sage_attn_fwd / sage_attn_fwd_ws call made by this thread records `before`
+ * sage_attn_fwd / _ws / _lse / _cross call made by this thread records `before`
  * on its stream immediately before launching its attention kernel and
  * `after` immediately after, so that the kernel's own duration can be read
  * with cudaEventElapsedTime.  Both are cudaEvent_t passed as void*, owned by

@@ -95,7 +95,7 @@ struct Params {
   uint16_t* out;
   int32_t* s_dump;
   float* lse;             // optional [B, H, S]
-  int S, H, S_pad, nb, n_kv, n_pairs;
+  int Sq, Skv, H, nbq, nbk, n_kv, n_pairs;   // query rows, key/value rows (equal unless cross)
   float c_scale;          // fp32(softmax_scale * fp32(log2 e))
   uint64_t timeout_ns;
 };
@@ -321,18 +321,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quarter = warp & 3;         // TMEM lane quarter of this warp
     const int row = quarter * 32 + lane;  // query row within the tile
     const int qrow = q_row0 + t * kTile + row;
-    const bool row_valid = qrow < p.S;
+    const bool row_valid = qrow < p.Sq;
     const uint32_t lane_bits = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t tS = tmem + lane_bits + col_s(t);
     const uint32_t tO = tmem + lane_bits + col_o(t);
-    const float* ksc = p.k_scale + static_cast<size_t>(bh) * p.nb;
-    const float sq = row_valid ? p.q_scale[static_cast<size_t>(bh) * p.nb + qrow / kQKBlock] : 0.0f;
+    const float* ksc = p.k_scale + static_cast<size_t>(bh) * p.nbk;
+    const float sq = row_valid ? p.q_scale[static_cast<size_t>(bh) * p.nbq + qrow / kQKBlock] : 0.0f;
     const float c_row = sq * p.c_scale;
 
     float m_run = -INFINITY;
     float sk_next[3];
 #pragma unroll
-    for (int i = 0; i < 3; ++i) sk_next[i] = i < p.nb ? __ldg(ksc + i) : 0.0f;
+    for (int i = 0; i < 3; ++i) sk_next[i] = i < p.nbk ? __ldg(ksc + i) : 0.0f;
     bool ok = true;
 
     for (int j = 0; j < p.n_kv; ++j) {
@@ -343,7 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < 3; ++i) {
           const int idx_k = 3 * (j + 1) + i;
-          sk_next[i] = idx_k < p.nb ? __ldg(ksc + idx_k) : 0.0f;
+          sk_next[i] = idx_k < p.nbk ? __ldg(ksc + idx_k) : 0.0f;
         }
       }
       // Warp-uniform outcome: the tcgen05 loads below are .sync.aligned.
@@ -371,13 +371,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(&bars.s_free[t]);
       if constexpr (kDumpS) {
         if (row_valid) {
-          int32_t* drow = p.s_dump + (static_cast<size_t>(bh) * p.S + qrow) * p.S + j * kKV;
-          const int lim = min(kKV, p.S - j * kKV);
+          int32_t* drow = p.s_dump + (static_cast<size_t>(bh) * p.Sq + qrow) * p.Skv + j * kKV;
+          const int lim = min(kKV, p.Skv - j * kKV);
           for (int c = 0; c < lim; ++c) drow[c] = __float2int_rn(a[c]);
         }
       }
 
-      const int valid = p.S - j * kKV;    // keys of this tile that exist (>= 1)
+      const int valid = p.Skv - j * kKV;  // keys of this tile that exist (>= 1)
       if (valid < kKV) {
 #pragma unroll
         for (int c = 0; c < kKV; ++c) a[c] = c < valid ? a[c] : -INFINITY;
@@ -448,9 +448,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float inv_l = 1.0f / __uint_as_float(l4[0]);
       // log sum_j exp(score_j) = ln 2 * (m + log2 L - log2 448): P~ = 448 at the max.
       if (p.lse != nullptr && row_valid)
-        p.lse[static_cast<size_t>(bh) * p.S + qrow] = (m_run + log2f(__uint_as_float(l4[0])) - kLog2P) * kLn2;
+        p.lse[static_cast<size_t>(bh) * p.Sq + qrow] = (m_run + log2f(__uint_as_float(l4[0])) - kLog2P) * kLn2;
       const int b = bh / p.H, h = bh % p.H;
-      uint16_t* orow = p.out + ((static_cast<size_t>(b) * p.S + qrow) * p.H + h) * kHeadDim;
+      uint16_t* orow = p.out + ((static_cast<size_t>(b) * p.Sq + qrow) * p.H + h) * kHeadDim;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t o[32];
@@ -527,9 +527,9 @@ __global__ void wait_timeout_probe_kernel(uint64_t timeout_ns) {
 cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream) {
   const uint64_t BH = static_cast<uint64_t>(a.B) * a.H;
   CUtensorMap tmQ, tmK, tmV;
-  if (!encode_map(&tmQ, a.q_codes, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, kHeadDim, a.S_pad, BH, 64, 128) ||
-      !encode_map(&tmK, a.k_codes, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, kHeadDim, a.S_pad, BH, 64, kKV) ||
-      !encode_map(&tmV, a.vt, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.S_pad, kHeadDim, BH, 128, 128))
+  if (!encode_map(&tmQ, a.q_codes, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, kHeadDim, a.Sq_pad, BH, 64, 128) ||
+      !encode_map(&tmK, a.k_codes, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, kHeadDim, a.Skv_pad, BH, 64, kKV) ||
+      !encode_map(&tmV, a.vt, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.Skv_pad, kHeadDim, BH, 128, 128))
     return cudaErrorInvalidValue;
   Params p;
   p.q_scale = a.q_scale;
@@ -538,12 +538,13 @@ cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream) {
   p.out = a.out;
   p.s_dump = a.s_dump;
   p.lse = a.lse;
-  p.S = a.S;
+  p.Sq = a.Sq;
+  p.Skv = a.Skv;
   p.H = a.H;
-  p.S_pad = a.S_pad;
-  p.nb = a.nb;
-  p.n_kv = (a.S + kKV - 1) / kKV;
-  p.n_pairs = (a.S_pad / kTile + 1) / 2;
+  p.nbq = a.nbq;
+  p.nbk = a.nbk;
+  p.n_kv = (a.Skv + kKV - 1) / kKV;
+  p.n_pairs = (a.Sq_pad / kTile + 1) / 2;
   p.c_scale = a.softmax_scale * kLog2e;
   p.timeout_ns = a.timeout_ns;
   const uint64_t grid = BH * static_cast<uint64_t>(p.n_pairs);

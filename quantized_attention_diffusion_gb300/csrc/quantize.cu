@@ -14,6 +14,7 @@
 //
 // This file is compiled without fast-math and without flush-to-zero: the
 // divisions are IEEE round-to-nearest-even (div.rn.f32).
+#include <algorithm>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -78,7 +79,8 @@ __global__ void __launch_bounds__(256) qk_quantize_kernel(QKQuantArgs<CodeT> a) 
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int sub = warp >> 2, w4 = warp & 3;
-  const int nbp = a.S_pad / 32;
+  const int S = a.S[tensor], S_pad = a.S_pad[tensor], nb = a.nb[tensor];
+  const int nbp = S_pad / 32;
   const long long gblk = static_cast<long long>(blockIdx.x) * 2 + sub;
   const bool active = gblk < static_cast<long long>(a.BH) * nbp;
   const int blk = active ? static_cast<int>(gblk % nbp) : 0;
@@ -88,14 +90,14 @@ __global__ void __launch_bounds__(256) qk_quantize_kernel(QKQuantArgs<CodeT> a) 
   const int c8 = (lane & 15) * 8;
   const int tok0 = blk * 32 + w4 * 8 + half;   // this lane's first token; then +2, +4, +6
   const size_t tok_stride = static_cast<size_t>(a.H) * kHeadDim;
-  const uint16_t* src = x + (static_cast<size_t>(b) * a.S * a.H + h) * kHeadDim + c8;
+  const uint16_t* src = x + (static_cast<size_t>(b) * S * a.H + h) * kHeadDim + c8;
 
   uint4 raw[4];
   float amax = 0.0f;
 #pragma unroll
   for (int it = 0; it < 4; ++it) {
     const int s = tok0 + 2 * it;
-    raw[it] = (active && s < a.S)
+    raw[it] = (active && s < S)
                   ? __ldcs(reinterpret_cast<const uint4*>(src + static_cast<size_t>(s) * tok_stride))
                   : make_uint4(0, 0, 0, 0);
     const uint32_t w[4] = {raw[it].x, raw[it].y, raw[it].z, raw[it].w};
@@ -111,9 +113,9 @@ __global__ void __launch_bounds__(256) qk_quantize_kernel(QKQuantArgs<CodeT> a) 
                fmaxf(warp_max[sub * 4 + 2], warp_max[sub * 4 + 3]));
   if (!active) return;
   const float sc = __fdiv_rn(amax, 127.0f);
-  if (w4 == 0 && lane == 0 && blk < a.nb) scale[static_cast<size_t>(bh) * a.nb + blk] = sc;
+  if (w4 == 0 && lane == 0 && blk < nb) scale[static_cast<size_t>(bh) * nb + blk] = sc;
 
-  CodeT* dst = codes + (static_cast<size_t>(bh) * a.S_pad + tok0) * kHeadDim + c8;
+  CodeT* dst = codes + (static_cast<size_t>(bh) * S_pad + tok0) * kHeadDim + c8;
 #pragma unroll
   for (int it = 0; it < 4; ++it) {
     const uint32_t w[4] = {raw[it].x, raw[it].y, raw[it].z, raw[it].w};
@@ -241,7 +243,7 @@ __global__ void __launch_bounds__(256) widen_codes_kernel(const int8_t* __restri
 
 template <typename CodeT>
 cudaError_t launch_qk_quantize(const QKQuantArgs<CodeT>& a, cudaStream_t stream) {
-  const long long blocks = static_cast<long long>(a.BH) * (a.S_pad / 32);
+  const long long blocks = static_cast<long long>(a.BH) * (std::max(a.S_pad[0], a.S_pad[1]) / 32);
   const long long ctas = (blocks + 1) / 2;
   qk_quantize_kernel<CodeT><<<dim3(static_cast<unsigned>(ctas), 2), 256, 0, stream>>>(a);
   return cudaGetLastError();

@@ -90,7 +90,7 @@ extern "C" sage_status sage_quantize_qkv_noalloc(const void* q, const void* k, c
   uint32_t* scratch = scratch_for_current_device();
   if (!scratch) return SAGE_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const int Sp = sage::padded_len(S), nb = sage::num_blocks(S);
+  const int Sp = sage::padded_len(S);
   sage::QKQuantArgs<int8_t> qa;
   qa.q = static_cast<const uint16_t*>(q);
   qa.k = static_cast<const uint16_t*>(k);
@@ -99,10 +99,8 @@ extern "C" sage_status sage_quantize_qkv_noalloc(const void* q, const void* k, c
   qa.q_scale = q_scale;
   qa.k_scale = k_scale;
   qa.BH = B * H;
-  qa.S = S;
   qa.H = H;
-  qa.S_pad = Sp;
-  qa.nb = nb;
+  qa.set_lengths(S, S);
   cudaError_t e = sage::launch_qk_quantize<int8_t>(qa, st);
   // launch_v_quantize zeroes the maxima (cudaMemsetAsync, no allocation)
   // before reducing into them, so the previous call's contents never leak.

@@ -69,15 +69,17 @@ struct WsLayout {
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
-WsLayout ws_layout(int B, int S, int H) {
-  const size_t BH = static_cast<size_t>(B) * H, Sp = padded_len(S), nb = num_blocks(S);
+// Sq query rows, Sk key/value rows (equal for self-attention).
+WsLayout ws_layout(int B, int Sq, int Sk, int H) {
+  const size_t BH = static_cast<size_t>(B) * H;
+  const size_t Sqp = padded_len(Sq), Skp = padded_len(Sk), nbq = num_blocks(Sq), nbk = num_blocks(Sk);
   WsLayout w;
   size_t off = 0;
-  w.q16 = off; off += align256(BH * Sp * kHeadDim * sizeof(__half));
-  w.k16 = off; off += align256(BH * Sp * kHeadDim * sizeof(__half));
-  w.vt = off; off += align256(BH * kHeadDim * Sp);
-  w.qs = off; off += align256(BH * nb * sizeof(float));
-  w.ks = off; off += align256(BH * nb * sizeof(float));
+  w.q16 = off; off += align256(BH * Sqp * kHeadDim * sizeof(__half));
+  w.k16 = off; off += align256(BH * Skp * kHeadDim * sizeof(__half));
+  w.vt = off; off += align256(BH * kHeadDim * Skp);
+  w.qs = off; off += align256(BH * nbq * sizeof(float));
+  w.ks = off; off += align256(BH * nbk * sizeof(float));
   w.vs = off; off += align256(BH * kHeadDim * sizeof(float));
   w.vamax = off; off += align256(BH * kHeadDim * sizeof(uint32_t));
   w.total = off;
@@ -121,10 +123,9 @@ cudaError_t pool_alloc(void** ptr, size_t bytes, cudaStream_t stream) {
 
 uint64_t timeout_ns() { return g_timeout_ns.load(std::memory_order_relaxed); }
 
-sage_status run_fused(const void* q, const void* k, const void* v, void* out, int B, int S, int H,
-                      float softmax_scale, void* ws, cudaStream_t st, float* lse = nullptr) {
-  const WsLayout w = ws_layout(B, S, H);
-  const int Sp = padded_len(S), nb = num_blocks(S);
+sage_status run_fused(const void* q, const void* k, const void* v, void* out, int B, int Sq, int Sk,
+                      int H, float softmax_scale, void* ws, cudaStream_t st, float* lse = nullptr) {
+  const WsLayout w = ws_layout(B, Sq, Sk, H);
   QKQuantArgs<__half> qa;
   qa.q = static_cast<const uint16_t*>(q);
   qa.k = static_cast<const uint16_t*>(k);
@@ -133,13 +134,11 @@ sage_status run_fused(const void* q, const void* k, const void* v, void* out, in
   qa.q_scale = at<float>(ws, w.qs);
   qa.k_scale = at<float>(ws, w.ks);
   qa.BH = B * H;
-  qa.S = S;
   qa.H = H;
-  qa.S_pad = Sp;
-  qa.nb = nb;
+  qa.set_lengths(Sq, Sk);
   cudaError_t e = launch_qk_quantize<__half>(qa, st);
   if (e != cudaSuccess) return cuda_fail(e, "Q/K quantisation launch");
-  e = launch_v_quantize(static_cast<const uint16_t*>(v), B, S, H, Sp, at<uint32_t>(ws, w.vamax),
+  e = launch_v_quantize(static_cast<const uint16_t*>(v), B, Sk, H, padded_len(Sk), at<uint32_t>(ws, w.vamax),
                         at<uint8_t>(ws, w.vt), at<float>(ws, w.vs), st);
   if (e != cudaSuccess) return cuda_fail(e, "V quantisation launch");
   AttnArgs aa;
@@ -153,10 +152,13 @@ sage_status run_fused(const void* q, const void* k, const void* v, void* out, in
   aa.s_dump = nullptr;
   aa.lse = lse;
   aa.B = B;
-  aa.S = S;
+  aa.Sq = Sq;
+  aa.Skv = Sk;
   aa.H = H;
-  aa.S_pad = Sp;
-  aa.nb = nb;
+  aa.Sq_pad = padded_len(Sq);
+  aa.Skv_pad = padded_len(Sk);
+  aa.nbq = num_blocks(Sq);
+  aa.nbk = num_blocks(Sk);
   aa.softmax_scale = softmax_scale;
   aa.timeout_ns = timeout_ns();
   if (t_attn_before && (e = cudaEventRecord(t_attn_before, st)) != cudaSuccess)
@@ -172,7 +174,7 @@ sage_status run_quantized(const int8_t* q_i8, const float* q_scale, const int8_t
                           const float* k_scale, const uint8_t* vt, const float* v_scale, void* out,
                           int32_t* s_dump, int B, int S, int H, float softmax_scale, void* ws,
                           cudaStream_t st) {
-  const WsLayout w = ws_layout(B, S, H);
+  const WsLayout w = ws_layout(B, S, S, H);
   const int Sp = padded_len(S);
   const size_t n = static_cast<size_t>(B) * H * Sp * kHeadDim;
   cudaError_t e = launch_widen_codes(q_i8, at<__half>(ws, w.q16), n, st);
@@ -189,10 +191,13 @@ sage_status run_quantized(const int8_t* q_i8, const float* q_scale, const int8_t
   aa.s_dump = s_dump;
   aa.lse = nullptr;
   aa.B = B;
-  aa.S = S;
+  aa.Sq = S;
+  aa.Skv = S;
   aa.H = H;
-  aa.S_pad = Sp;
-  aa.nb = num_blocks(S);
+  aa.Sq_pad = Sp;
+  aa.Skv_pad = Sp;
+  aa.nbq = num_blocks(S);
+  aa.nbk = num_blocks(S);
   aa.softmax_scale = softmax_scale;
   aa.timeout_ns = timeout_ns();
   e = launch_attention(aa, st);
@@ -201,7 +206,7 @@ sage_status run_quantized(const int8_t* q_i8, const float* q_scale, const int8_t
 }
 
 sage_status check_workspace(void* ws, size_t bytes, int B, int S, int H) {
-  const size_t need = ws_layout(B, S, H).total;
+  const size_t need = ws_layout(B, S, S, H).total;
   if (!ws) return fail(SAGE_ERR_INVALID_ARG, "workspace is NULL");
   if (!aligned(ws, 256)) return fail(SAGE_ERR_MISALIGNED, "workspace is not 256-byte aligned");
   if (bytes < need)
@@ -227,7 +232,7 @@ int64_t sage_padded_len(int S) { return S < 1 ? 0 : static_cast<int64_t>(padded_
 size_t sage_workspace_bytes(int B, int S, int H, int D) {
   if (D != kHeadDim || B < 1 || S < 1 || H < 1 || static_cast<int64_t>(B) * H > INT_MAX || S > (1 << 28))
     return 0;
-  return ws_layout(B, S, H).total;
+  return ws_layout(B, S, S, H).total;
 }
 
 sage_status sage_quantize_qkv(const void* q, const void* k, const void* v, int B, int S, int H, int D,
@@ -239,7 +244,7 @@ sage_status sage_quantize_qkv(const void* q, const void* k, const void* v, int B
                     {k_scale, "k_scale"}, {vt_fp8, "vt_fp8"}, {v_scale, "v_scale"}});
   if (s != SAGE_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const int Sp = padded_len(S), nb = num_blocks(S);
+  const int Sp = padded_len(S);
   QKQuantArgs<int8_t> qa;
   qa.q = static_cast<const uint16_t*>(q);
   qa.k = static_cast<const uint16_t*>(k);
@@ -248,10 +253,8 @@ sage_status sage_quantize_qkv(const void* q, const void* k, const void* v, int B
   qa.q_scale = q_scale;
   qa.k_scale = k_scale;
   qa.BH = B * H;
-  qa.S = S;
   qa.H = H;
-  qa.S_pad = Sp;
-  qa.nb = nb;
+  qa.set_lengths(S, S);
   cudaError_t e = launch_qk_quantize<int8_t>(qa, st);
   if (e != cudaSuccess) return cuda_fail(e, "Q/K quantisation launch");
   void* scratch = nullptr;
@@ -273,7 +276,7 @@ sage_status sage_attn_fwd_ws(const void* q, const void* k, const void* v, void* 
   if (s == SAGE_OK) s = check_ptrs({{q, "q"}, {k, "k"}, {v, "v"}, {out, "out"}});
   if (s == SAGE_OK) s = check_workspace(workspace, workspace_bytes, B, S, H);
   if (s != SAGE_OK) return s;
-  return run_fused(q, k, v, out, B, S, H, softmax_scale, workspace, static_cast<cudaStream_t>(stream));
+  return run_fused(q, k, v, out, B, S, S, H, softmax_scale, workspace, static_cast<cudaStream_t>(stream));
 }
 
 sage_status sage_attn_fwd(const void* q, const void* k, const void* v, void* out, int B, int S, int H,
@@ -284,11 +287,11 @@ sage_status sage_attn_fwd(const void* q, const void* k, const void* v, void* out
   if (s != SAGE_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   void* ws = nullptr;
-  cudaError_t e = pool_alloc(&ws, ws_layout(B, S, H).total, st);
+  cudaError_t e = pool_alloc(&ws, ws_layout(B, S, S, H).total, st);
   if (e != cudaSuccess)
-    return fail(SAGE_ERR_NO_MEMORY, "workspace allocation of %zu bytes failed: %s", ws_layout(B, S, H).total,
+    return fail(SAGE_ERR_NO_MEMORY, "workspace allocation of %zu bytes failed: %s", ws_layout(B, S, S, H).total,
                 cudaGetErrorString(e));
-  s = run_fused(q, k, v, out, B, S, H, softmax_scale, ws, st);
+  s = run_fused(q, k, v, out, B, S, S, H, softmax_scale, ws, st);
   e = cudaFreeAsync(ws, st);
   if (s != SAGE_OK) return s;
   if (e != cudaSuccess) return cuda_fail(e, "workspace release");
@@ -303,11 +306,32 @@ sage_status sage_attn_fwd_lse(const void* q, const void* k, const void* v, void*
   if (s != SAGE_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   void* ws = nullptr;
-  cudaError_t e = pool_alloc(&ws, ws_layout(B, S, H).total, st);
+  cudaError_t e = pool_alloc(&ws, ws_layout(B, S, S, H).total, st);
   if (e != cudaSuccess)
-    return fail(SAGE_ERR_NO_MEMORY, "workspace allocation of %zu bytes failed: %s", ws_layout(B, S, H).total,
+    return fail(SAGE_ERR_NO_MEMORY, "workspace allocation of %zu bytes failed: %s", ws_layout(B, S, S, H).total,
                 cudaGetErrorString(e));
-  s = run_fused(q, k, v, out, B, S, H, softmax_scale, ws, st, lse);
+  s = run_fused(q, k, v, out, B, S, S, H, softmax_scale, ws, st, lse);
+  e = cudaFreeAsync(ws, st);
+  if (s != SAGE_OK) return s;
+  if (e != cudaSuccess) return cuda_fail(e, "workspace release");
+  return SAGE_OK;
+}
+
+sage_status sage_attn_fwd_cross(const void* q, const void* k, const void* v, void* out, float* lse, int B,
+                                int Sq, int Skv, int H, int D, float softmax_scale, void* stream) {
+  sage_status s = check_shape(B, Sq, H, D);
+  if (s == SAGE_OK) s = check_shape(B, Skv, H, D);
+  if (s == SAGE_OK) s = check_scale(softmax_scale);
+  if (s == SAGE_OK) s = check_ptrs({{q, "q"}, {k, "k"}, {v, "v"}, {out, "out"}});
+  if (s == SAGE_OK && lse) s = check_ptrs({{lse, "lse"}});
+  if (s != SAGE_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t bytes = ws_layout(B, Sq, Skv, H).total;
+  void* ws = nullptr;
+  cudaError_t e = pool_alloc(&ws, bytes, st);
+  if (e != cudaSuccess)
+    return fail(SAGE_ERR_NO_MEMORY, "workspace allocation of %zu bytes failed: %s", bytes, cudaGetErrorString(e));
+  s = run_fused(q, k, v, out, B, Sq, Skv, H, softmax_scale, ws, st, lse);
   e = cudaFreeAsync(ws, st);
   if (s != SAGE_OK) return s;
   if (e != cudaSuccess) return cuda_fail(e, "workspace release");

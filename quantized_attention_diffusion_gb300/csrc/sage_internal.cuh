@@ -28,7 +28,12 @@ struct QKQuantArgs {
   CodeT* k_codes;
   float* q_scale;      // [B, H, nb]
   float* k_scale;
-  int BH, S, H, S_pad, nb;
+  int BH, H;
+  int S[2], S_pad[2], nb[2];   // per tensor: [0] Q, [1] K (cross-attention: they differ)
+  void set_lengths(int Sq, int Sk) {
+    S[0] = Sq; S_pad[0] = padded_len(Sq); nb[0] = num_blocks(Sq);
+    S[1] = Sk; S_pad[1] = padded_len(Sk); nb[1] = num_blocks(Sk);
+  }
 };
 
 template <typename CodeT>
@@ -44,13 +49,13 @@ struct AttnArgs {
   const __half* q_codes;    // integer-valued fp16 codes [B, H, S_pad, 128]
   const __half* k_codes;
   const uint8_t* vt;        // e4m3 V^T [B, H, 128, S_pad]
-  const float* q_scale;     // [B, H, nb]
-  const float* k_scale;
+  const float* q_scale;     // [B, H, nbq]
+  const float* k_scale;     // [B, H, nbk]
   const float* v_scale;     // [B, H, 128]
-  uint16_t* out;            // bf16 [B, S, H, 128]
-  int32_t* s_dump;          // optional int32 Q K^T [B, H, S, S] (debug entry only)
-  float* lse;               // optional fp32 [B, H, S]: per-row log-sum-exp
-  int B, S, H, S_pad, nb;
+  uint16_t* out;            // bf16 [B, Sq, H, 128]
+  int32_t* s_dump;          // optional int32 Q K^T [B, H, Sq, Skv] (debug entry only)
+  float* lse;               // optional fp32 [B, H, Sq]: per-row log-sum-exp
+  int B, Sq, Skv, H, Sq_pad, Skv_pad, nbq, nbk;   // Q rows / K,V rows (equal unless cross)
   float softmax_scale;
   uint64_t timeout_ns;
 };

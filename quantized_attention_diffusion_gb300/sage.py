@@ -33,7 +33,7 @@ EXPORTED = (
     "sage_attn_fwd_ws", "sage_attn_fwd_quantized", "sage_debug_qk_int32",
     "sage_debug_wait_timeout", "sage_sync_status", "sage_set_wait_timeout_ns",
     "sage_last_error", "sage_status_string", "sage_set_attention_events",
-    "sage_quantize_qkv_noalloc", "sage_attn_fwd_lse",
+    "sage_quantize_qkv_noalloc", "sage_attn_fwd_lse", "sage_attn_fwd_cross",
 )
 
 
@@ -70,6 +70,7 @@ def load_library(path: str = LIB_PATH):
             "sage_attn_fwd": (S, [P, P, P, P, I, I, I, I, F, P]),
             "sage_attn_fwd_ws": (S, [P, P, P, P, I, I, I, I, F, P, Z, P]),
             "sage_attn_fwd_lse": (S, [P, P, P, P, P, I, I, I, I, F, P]),
+            "sage_attn_fwd_cross": (S, [P, P, P, P, P, I, I, I, I, I, F, P]),
             "sage_attn_fwd_quantized": (S, [P, P, P, P, P, P, P, I, I, I, I, F, P, Z, P]),
             "sage_debug_qk_int32": (S, [P, P, P, P, P, P, P, P, I, I, I, I, F, P, Z, P]),
             "sage_debug_wait_timeout": (S, [ctypes.c_uint64, P]),
@@ -175,6 +176,39 @@ def attn_fwd_lse(q, k, v, softmax_scale: float | None = None, out=None, lse=None
         _check(lib.sage_attn_fwd_lse(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, S, H, D,
                                      float(softmax_scale), _stream(q.device)))
     return out, lse
+
+
+def attn_fwd_cross(q, k, v, softmax_scale: float | None = None, out=None, lse=None,
+                   return_lse: bool = False):
+    """Cross-attention: q bf16 [B, Sq, H, 128], k and v bf16 [B, Skv, H, 128]
+    -> out bf16 [B, Sq, H, 128] (and lse fp32 [B, H, Sq] with return_lse or
+    when ``lse`` is given), through sage_attn_fwd_cross."""
+    lib = load_library()
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor) or t.dtype != torch.bfloat16 or not t.is_cuda \
+                or not t.is_contiguous() or t.dim() != 4:
+            raise ValueError(f"{name} must be a contiguous bf16 CUDA tensor [B, S, H, D]")
+    B, Sq, H, D = q.shape
+    if k.shape != v.shape or k.shape[0] != B or k.shape[2] != H or k.shape[3] != D:
+        raise ValueError(f"k and v must be [B, Skv, H, D] with B, H, D of q; got {tuple(k.shape)}, "
+                         f"{tuple(v.shape)} for q {tuple(q.shape)}")
+    if k.device != q.device or v.device != q.device:
+        raise ValueError("q, k and v must be on one device")
+    Skv = k.shape[1]
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((B, H, Sq), dtype=torch.float32, device=q.device)
+    if lse is not None and (lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, Sq)
+                            or not lse.is_contiguous() or lse.device != q.device):
+        raise ValueError("lse must be a contiguous float32 [B, H, Sq] tensor on q's device")
+    with torch.cuda.device(q.device):
+        _check(lib.sage_attn_fwd_cross(_ptr(q), _ptr(k), _ptr(v), _ptr(out),
+                                       _ptr(lse) if lse is not None else None, B, Sq, Skv, H, D,
+                                       float(softmax_scale), _stream(q.device)))
+    return (out, lse) if lse is not None else out
 
 
 def quantize_qkv(q, k, v, out=None, noalloc=False):

@@ -3,7 +3,8 @@
 This module draws the BF16 inputs that both the CUDA path and the CPU oracle
 consume.  It holds none of the attention method's arithmetic: it only samples
 normal variates and shapes them like the pages' diffusion and video
-workloads (equal Q/K/V shapes ``[B, S, H, 128]``, BF16).
+workloads (Q/K/V ``[B, S, H, 128]``, BF16; K and V may have their own
+length Skv for cross-attention).
 
 Recipes (each input is drawn fp32 from one ``torch.Generator`` seeded per
 workload, in the order Q, K, V, then the recipe's extra draws, and rounded to
@@ -36,6 +37,11 @@ class Workload:
     recipe: str
     seed: int
     D: int = HEAD_DIM
+    Skv: int | None = None      # keys/values; None: self-attention (Skv = S)
+
+    @property
+    def skv(self) -> int:
+        return self.S if self.Skv is None else self.Skv
 
     @property
     def softmax_scale(self) -> float:
@@ -43,11 +49,12 @@ class Workload:
 
     @property
     def ops(self) -> int:
-        """Tensor operations of one attention call: 4 * B * H * S^2 * D."""
-        return 4 * self.B * self.H * self.S * self.S * self.D
+        """Tensor operations of one attention call: 4 * B * H * S * Skv * D."""
+        return 4 * self.B * self.H * self.S * self.skv * self.D
 
     def describe(self) -> str:
-        return f"B={self.B} S={self.S} H={self.H} D={self.D} {self.recipe} seed={self.seed}"
+        kv = "" if self.Skv is None else f" Skv={self.Skv}"
+        return f"B={self.B} S={self.S}{kv} H={self.H} D={self.D} {self.recipe} seed={self.seed}"
 
 
 # The pages' workloads, by what they are.
@@ -59,25 +66,31 @@ WORKLOADS = {
         Workload("b2_s16384_h24_outlier", 2, 16384, 24, "qk_outlier_channels", 2),
         Workload("b1_s32760_h40", 1, 32760, 40, "normal", 3),
         Workload("b1_s65536_h24_koffset", 1, 65536, 24, "k_channel_offset", 4),
+        # cross-attention: image tokens attending to a short, ragged text context,
+        # and a short query block against a long key/value sequence
+        Workload("b2_sq16384_skv333_h24_cross", 2, 16384, 24, "normal", 5, Skv=333),
+        Workload("b1_sq4096_skv16384_h24_cross", 1, 4096, 24, "k_channel_offset", 6, Skv=16384),
     ]
 }
 
 
 def make_qkv(B: int, S: int, H: int, D: int = HEAD_DIM, recipe: str = "normal",
-             seed: int = 0, device: str | torch.device = "cpu"):
-    """Return (q, k, v) BF16 tensors of shape [B, S, H, D] on ``device``.
+             seed: int = 0, device: str | torch.device = "cpu", Skv: int | None = None):
+    """Return (q, k, v) BF16 tensors on ``device``: q [B, S, H, D], k and v
+    [B, Skv, H, D] (Skv defaults to S).
 
     Values are drawn on the CPU so that a workload has the same bytes on
     every device; the tensors are then copied.
     """
     g = torch.Generator(device="cpu").manual_seed(int(seed))
+    Skv = S if Skv is None else int(Skv)
 
-    def draw():
-        return torch.randn((B, S, H, D), generator=g, dtype=torch.float32)
+    def draw(n):
+        return torch.randn((B, n, H, D), generator=g, dtype=torch.float32)
 
-    q = draw()
-    k = draw()
-    v = draw()
+    q = draw(S)
+    k = draw(Skv)
+    v = draw(Skv)
     if recipe == "k_channel_offset":
         offset = torch.randn((H, D), generator=g, dtype=torch.float32) * 2.0
         k += offset.view(1, 1, H, D)
@@ -95,7 +108,7 @@ def make_qkv(B: int, S: int, H: int, D: int = HEAD_DIM, recipe: str = "normal",
 
 
 def make_workload(w: Workload, device="cpu"):
-    return make_qkv(w.B, w.S, w.H, w.D, w.recipe, w.seed, device)
+    return make_qkv(w.B, w.S, w.H, w.D, w.recipe, w.seed, device, Skv=w.Skv)
 
 
 def bf16_bits(t: torch.Tensor):
