@@ -66,6 +66,7 @@ def _load():
         lib.oracle_e4m3_decode_array.argtypes = [P, ctypes.c_int64, P]
         lib.oracle_quantize_qk.argtypes = [P, I, I, I, I, I, P, P]
         lib.oracle_quantize_v.argtypes = [P, I, I, I, I, I, P, P]
+        lib.oracle_quantize_k_smooth.argtypes = [P, I, I, I, I, I, P, P, P]
         lib.oracle_qk_int32.restype = I
         lib.oracle_qk_int32.argtypes = [P, P, I, I, I, I, I, P]
         lib.oracle_attend_rows.restype = I
@@ -214,16 +215,31 @@ def attend_row_debug(quant, S: int, softmax_scale: float, b: int, h: int, i: int
     return out, pc, L.value
 
 
-def quantize(q: np.ndarray, k: np.ndarray, v: np.ndarray):
-    """The three quantisation steps: returns (qc, qs, kc, ks, vt, vs)."""
+def quantize_k_smooth(k: np.ndarray):
+    """K smoothing then quantisation (reading R15): returns (codes int8
+    [B, H, S_pad, D], scales fp32 [B, H, nb], channel means fp32 [B, H, D])."""
+    k = np.ascontiguousarray(k, dtype=np.uint16)
+    B, S, H, D = k.shape
+    Sp = padded_len(S)
+    codes = np.empty((B, H, Sp, D), dtype=np.int8)
+    scale = np.empty((B, H, (S + 31) // 32), dtype=np.float32)
+    mean = np.empty((B, H, D), dtype=np.float32)
+    _load().oracle_quantize_k_smooth(_ptr(k), B, S, H, D, Sp, _ptr(codes), _ptr(scale), _ptr(mean))
+    return codes, scale, mean
+
+
+def quantize(q: np.ndarray, k: np.ndarray, v: np.ndarray, smooth_k: bool = False):
+    """The three quantisation steps: returns (qc, qs, kc, ks, vt, vs); with
+    smooth_k, K is smoothed first (R15)."""
     qc, qs = quantize_qk(q)
-    kc, ks = quantize_qk(k)
+    kc, ks = quantize_k_smooth(k)[:2] if smooth_k else quantize_qk(k)
     vt, vs = quantize_v(v)
     return qc, qs, kc, ks, vt, vs
 
 
 def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, softmax_scale: float,
-              rows: np.ndarray | None = None, l_mode: int = 0, return_ties: bool = False):
+              rows: np.ndarray | None = None, l_mode: int = 0, return_ties: bool = False,
+              smooth_k: bool = False):
     """Whole quantize-then-attend path from bf16 bits.
 
     rows None: full output bf16 bits [B,S,H,D] (ties [B,S,H]); otherwise
@@ -231,7 +247,7 @@ def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, softmax_scale: float,
     """
     B, S, H, D = q.shape
     Skv = k.shape[1]
-    quant = quantize(q, k, v)
+    quant = quantize(q, k, v, smooth_k=smooth_k)
     if rows is None:
         out, ties = attend_rows(quant, S, softmax_scale, all_rows(B, S, H), l_mode, True, Skv=Skv)
         out, ties = out.reshape(B, S, H, D), ties.reshape(B, S, H)

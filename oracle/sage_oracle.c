@@ -55,6 +55,13 @@
  *      the natural log of sum_j exp(scores) as this quantised computation
  *      estimates it (p_j = 448 * 2^(x_j - m), so sum_j 2^(x_j) ~ 2^m L / 448).
  *      Tie bound for lse: ln(L / (L - T)).
+ *  R15 (K smoothing, optional) before K is quantised, each (batch, head,
+ *      channel d) of K loses its mean over the S tokens: mean_d =
+ *      fp32(sum_s k_sd / S), the sum taken in double (exact for bf16 inputs
+ *      whose magnitudes span fewer than 45 - log2 S binary orders) and the
+ *      division in double, rounded once; k'_sd = fl32(k_sd - mean_d); k' is
+ *      then quantised as R1/R2.  Every score of a query row moves by the
+ *      same q . mean, so the softmax is unchanged in exact arithmetic.
  *  R14 (cross-attention) Q may have Sq rows and K, V S != Sq rows: each is
  *      quantised over its own 32-row blocks (Q, K) or its own tokens (V);
  *      every step above runs over the S keys unchanged.
@@ -316,6 +323,47 @@ static void attend_row(const int8_t *q, const float *qs, const int8_t *k,
     /* R13 */
     if (lse_out) *lse_out = log(2.0) * ((double)m_run + log2(L) - log2(448.0));
     if (lse_tie_out) *lse_tie_out = (T > 0.0 && L > T) ? log(L / (L - T)) : (T > 0.0 ? INFINITY : 0.0);
+}
+
+/* K smoothing (R15): per (b, h) channel means over the S tokens (fp32,
+ * [B, H, D]) and INT8 codes / block scales of k - mean, layouts as
+ * oracle_quantize_qk. */
+void oracle_quantize_k_smooth(const uint16_t *x, int B, int S, int H, int D,
+                              int S_pad, int8_t *codes, float *scale, float *mean) {
+    int nb = (S + 31) / 32;
+#pragma omp parallel for collapse(2) schedule(static)
+    for (int b = 0; b < B; ++b)
+        for (int h = 0; h < H; ++h) {
+            float *mu = mean + ((size_t)b * H + h) * D;
+            for (int d = 0; d < D; ++d) {
+                double sum = 0.0;
+                for (int s = 0; s < S; ++s)
+                    sum += (double)bf16_to_f32(x[(((size_t)b * S + s) * H + h) * D + d]);
+                mu[d] = (float)(sum / (double)S);
+            }
+            int8_t *dst = codes + ((size_t)b * H + h) * S_pad * D;
+            memset(dst, 0, (size_t)S_pad * D);
+            for (int blk = 0; blk < nb; ++blk) {
+                int r0 = blk * 32, r1 = r0 + 32 < S ? r0 + 32 : S;
+                float amax = 0.0f;
+                for (int s = r0; s < r1; ++s)
+                    for (int d = 0; d < D; ++d) {
+                        float v = bf16_to_f32(x[(((size_t)b * S + s) * H + h) * D + d]) - mu[d];
+                        if (fabsf(v) > amax) amax = fabsf(v);
+                    }
+                float sc = amax / 127.0f;
+                scale[((size_t)b * H + h) * nb + blk] = sc;
+                if (sc == 0.0f) continue;
+                for (int s = r0; s < r1; ++s)
+                    for (int d = 0; d < D; ++d) {
+                        float v = bf16_to_f32(x[(((size_t)b * S + s) * H + h) * D + d]) - mu[d];
+                        float r = rintf(v / sc);
+                        if (r > 127.0f) r = 127.0f;
+                        if (r < -127.0f) r = -127.0f;
+                        dst[(size_t)s * D + d] = (int8_t)r;
+                    }
+            }
+        }
 }
 
 /* Decode one head's V^T codes into [S][D] floats (e4m3 values are exact in
