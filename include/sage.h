@@ -171,6 +171,30 @@ sage_status sage_attn_fwd_cross(const void* q, const void* k, const void* v, voi
                                 int Sq, int Skv, int H, int D, float softmax_scale, void* stream);
 
 /*
+ * sage_attn_fwd_fused_q -- sage_attn_fwd with Q quantised inside the
+ * attention kernel, as the pages' kernel does (issue #15014, contract
+ * bullet "quantized per 32-row block ... inside the kernel"): the kernel
+ * loads bf16 Q and each softmax warp quantises its own 32-row block before
+ * the first QK^T; only K and V go through the separate quantisation pass.
+ * Same arguments, results (bit for bit) and errors as sage_attn_fwd.  On
+ * GB300 it is slower than sage_attn_fwd: the in-kernel quantisation sits on
+ * every CTA's critical path ahead of its first MMA.
+ */
+sage_status sage_attn_fwd_fused_q(const void* q, const void* k, const void* v, void* out, int B, int S,
+                                  int H, int D, float softmax_scale, void* stream);
+
+/*
+ * sage_debug_fused_q -- sage_attn_fwd_fused_q that also writes out the Q
+ * codes and block scales its attention kernel computed.
+ *   q_i8     out: int8 [B, H, S_pad, D] (rows >= S are 0)
+ *   q_scale  out: fp32 [B, H, nb]
+ * Same values sage_quantize_qkv writes for Q; for tests.  Errors as
+ * sage_attn_fwd.
+ */
+sage_status sage_debug_fused_q(const void* q, const void* k, const void* v, void* out, int B, int S, int H,
+                               int D, float softmax_scale, int8_t* q_i8, float* q_scale, void* stream);
+
+/*
  * sage_attn_fwd_quantized -- the attention step alone, from operands in the
  * layouts sage_quantize_qkv() writes (same passage as sage_attn_fwd).
  * `workspace` (caller-owned, >= sage_workspace_bytes) receives fp16 copies of

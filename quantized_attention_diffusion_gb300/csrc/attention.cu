@@ -89,6 +89,10 @@ constexpr uint32_t kE4M3One = 0x38383838u;                // four E4M3 1.0
 static_assert(kSmemDynamic <= 227 * 1024 - 1024, "shared memory budget");
 
 struct Params {
+  int fuse_q;             // 1: Q arrives as bf16 and is quantised here (q_scale unused)
+  int8_t* q_dump;         // optional with fuse_q: the Q codes, int8 [B, H, Sq_pad, 128]
+  float* q_scale_dump;    // optional with fuse_q: the Q block scales [B, H, nbq]
+  int Sq_pad;
   const float* q_scale;
   const float* k_scale;
   const float* v_scale;
@@ -101,7 +105,7 @@ struct Params {
 };
 
 struct Barriers {
-  uint64_t q_full;
+  uint64_t q_full, q_ready;
   uint64_t k_full[kStages], k_empty[kStages];
   uint64_t v_full[kStages], v_empty[kStages];
   uint64_t s_full[2], s_free[2], p_full[2], pv_done[2], o_full[2];
@@ -160,6 +164,73 @@ __device__ __forceinline__ void store_p_row(uint8_t* tile, int r, const uint32_t
         make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
 }
 
+// INT8 code of x for block scale sc, bit-identical to clamp(rint(x / sc),
+// -127, 127) with x / sc rounded to nearest even in fp32.  While 1/sc is a
+// normal float (sc in [2^-125, 2^125]), y = x * fl(1/sc) is within
+// |x/sc| * 2^-23 <= 1.6e-5 of x/sc (|x/sc| <= 127) and fl(x/sc) within
+// 7.6e-6, so both round to the same integer unless y lies within 2^-15 of a
+// half-integer; only then, or for extreme scales, is the division done.
+__device__ __forceinline__ int q_code(float x, float sc, float rcp) {
+  if (sc == 0.0f) return 0;
+  float y;
+  if (sc >= 0x1p-125f && sc <= 0x1p125f) {
+    y = x * rcp;
+    if (fabsf(y - floorf(y) - 0.5f) < 0x1p-15f) y = __fdiv_rn(x, sc);
+  } else {
+    y = __fdiv_rn(x, sc);
+  }
+  return static_cast<int>(fminf(fmaxf(rintf(y), -127.0f), 127.0f));
+}
+
+// One lane per row: quantise row r (0..127) of a bf16 Q tile in shared
+// memory (two 64-column halves, 128-byte swizzled rows) in place to
+// integer-valued fp16 codes.  The 32 lanes of the warp are one 32-row block:
+// scale = amax / 127 over the block (fp32 RNE division).  Two passes over
+// the row (max, then codes) keep few registers live.  Returns the scale.
+__device__ __forceinline__ float quantize_q_rows(uint8_t* tile, int r, int bh, int tile_row0, int8_t* q_dump,
+                                                 float* q_scale_dump, int Sq_pad, int nbq) {
+  const uint32_t roff = static_cast<uint32_t>((r >> 3) * 1024 + (r & 7) * 128);
+  float amax = 0.0f;
+#pragma unroll 4
+  for (int i = 0; i < 16; ++i) {
+    const int hf = i >> 3, c = i & 7;
+    const uint4 ch = *reinterpret_cast<const uint4*>(tile + hf * kQHalf + roff + ((c ^ (r & 7)) << 4));
+    const uint32_t w[4] = {ch.x, ch.y, ch.z, ch.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(w[e] << 16)), fabsf(__uint_as_float(w[e] & 0xFFFF0000u))));
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
+  const float sc = __fdiv_rn(amax, 127.0f);
+  const float rcp = __frcp_rn(sc);
+  const int grow = tile_row0 + r;
+  int8_t* dump = (q_dump != nullptr && grow < Sq_pad)
+                     ? q_dump + (static_cast<size_t>(bh) * Sq_pad + grow) * kHeadDim : nullptr;
+#pragma unroll 2
+  for (int i = 0; i < 16; ++i) {
+    const int hf = i >> 3, c = i & 7;
+    uint4* cp = reinterpret_cast<uint4*>(tile + hf * kQHalf + roff + ((c ^ (r & 7)) << 4));
+    const uint4 ch = *cp;
+    const uint32_t w[4] = {ch.x, ch.y, ch.z, ch.w};
+    uint32_t h2[4], b4[2] = {0u, 0u};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int lo = q_code(__uint_as_float(w[e] << 16), sc, rcp);
+      const int hi = q_code(__uint_as_float(w[e] & 0xFFFF0000u), sc, rcp);
+      const __half2 hh = __halves2half2(__int2half_rn(lo), __int2half_rn(hi));
+      h2[e] = *reinterpret_cast<const uint32_t*>(&hh);
+      b4[e >> 1] |= ((static_cast<uint32_t>(lo) & 0xFFu) | ((static_cast<uint32_t>(hi) & 0xFFu) << 8)) << (16 * (e & 1));
+    }
+    *cp = make_uint4(h2[0], h2[1], h2[2], h2[3]);
+    if (dump) *reinterpret_cast<uint2*>(dump + hf * 64 + c * 8) = make_uint2(b4[0], b4[1]);
+  }
+  const int blk = (tile_row0 + (r & ~31)) / kQKBlock;
+  if (q_scale_dump != nullptr && (r & 31) == 0 && blk < nbq)
+    q_scale_dump[static_cast<size_t>(bh) * nbq + blk] = sc;
+  return sc;
+}
+
 template <bool kDumpS>
 __global__ void __launch_bounds__(kThreads, 1)
     sage_attn_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -184,6 +255,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(&bars.q_full, 1);
+    mbar_init(&bars.q_ready, 256);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&bars.k_full[s], 1);
       mbar_init(&bars.k_empty[s], 1);
@@ -229,8 +301,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       mbar_arrive_expect_tx(&bars.q_full, 2 * kQTileBytes);
       for (int t = 0; t < 2; ++t) {
-        tma_load_3d(sQ + t * kQTileBytes, &tmQ, &bars.q_full, 0, q_row0 + t * kTile, bh);
-        tma_load_3d(sQ + t * kQTileBytes + kQHalf, &tmQ, &bars.q_full, 64, q_row0 + t * kTile, bh);
+        if (p.fuse_q) {   // bf16 [B, S, H, 128]: box of 64 channels x 128 tokens of one (b, h)
+          const int b = bh / p.H, h = bh % p.H;
+          tma_load_4d(sQ + t * kQTileBytes, &tmQ, &bars.q_full, 0, h, q_row0 + t * kTile, b);
+          tma_load_4d(sQ + t * kQTileBytes + kQHalf, &tmQ, &bars.q_full, 64, h, q_row0 + t * kTile, b);
+        } else {
+          tma_load_3d(sQ + t * kQTileBytes, &tmQ, &bars.q_full, 0, q_row0 + t * kTile, bh);
+          tma_load_3d(sQ + t * kQTileBytes + kQHalf, &tmQ, &bars.q_full, 64, q_row0 + t * kTile, bh);
+        }
       }
       int k_issued = 0, v_issued = 0;
       for (int j = 0; j < p.n_kv; ++j) {
@@ -257,7 +335,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const uint32_t idesc = make_idesc_f32acc(128, kKV, 0, 0);   // F16 x F16 -> F32
       const uint32_t q_lo = sw128_desc_lo(smem_addr(sQ)), k_lo = sw128_desc_lo(smem_addr(sK));
-      if (wait_bar(&bars.q_full, 0, abort_v, p.timeout_ns)) {
+      // Q codes: straight from TMA, or after the softmax warps quantised them.
+      if (wait_bar(p.fuse_q ? &bars.q_ready : &bars.q_full, 0, abort_v, p.timeout_ns)) {
         for (int j = 0; j < p.n_kv; ++j) {
           const int s = j % kStages;
           if (!wait_bar(&bars.k_full[s], (j / kStages) & 1, abort_v, p.timeout_ns)) break;
@@ -326,16 +405,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tS = tmem + lane_bits + col_s(t);
     const uint32_t tO = tmem + lane_bits + col_o(t);
     const float* ksc = p.k_scale + static_cast<size_t>(bh) * p.nbk;
-    const float sq = row_valid ? p.q_scale[static_cast<size_t>(bh) * p.nbq + qrow / kQKBlock] : 0.0f;
+    float sq = 0.0f;
+    bool ok = true;
+    if (p.fuse_q) {
+      // Quantise this warp's own 32 rows of Q (one K-block-sized Q block, the
+      // rows its softmax serves) in place: bf16 in, integer-valued fp16 out.
+      ok = __all_sync(0xFFFFFFFFu, wait_bar(&bars.q_full, 0, abort_v, p.timeout_ns));
+      if (ok)
+        sq = quantize_q_rows(sQ + t * kQTileBytes, row, bh, q_row0 + t * kTile, p.q_dump, p.q_scale_dump,
+                             p.Sq_pad, p.nbq);
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // codes visible to the MMA
+      mbar_arrive(&bars.q_ready);
+    } else {
+      sq = row_valid ? p.q_scale[static_cast<size_t>(bh) * p.nbq + qrow / kQKBlock] : 0.0f;
+    }
     const float c_row = sq * p.c_scale;
 
     float m_run = -INFINITY;
     float sk_next[3];
 #pragma unroll
     for (int i = 0; i < 3; ++i) sk_next[i] = i < p.nbk ? __ldg(ksc + i) : 0.0f;
-    bool ok = true;
 
-    for (int j = 0; j < p.n_kv; ++j) {
+    for (int j = 0; j < (ok ? p.n_kv : 0); ++j) {
       float cb[3];
 #pragma unroll
       for (int i = 0; i < 3; ++i) cb[i] = c_row * sk_next[i];
@@ -509,6 +600,25 @@ bool encode_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, uint32
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 4-D map over bf16 [B, S, H, 128] with a box of 64 channels x 1 head x 128
+// tokens x 1 batch and 128-byte swizzle: one half of a 128-row Q tile of one
+// (batch, head).  Tokens past S read as zeros.
+bool encode_map_bshd(CUtensorMap* m, const void* base, int B, int S, int H) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  std::memset(m, 0, sizeof(*m));
+  const cuuint64_t e = 2;
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(S),
+                        static_cast<cuuint64_t>(B)};
+  cuuint64_t strides[3] = {kHeadDim * e, static_cast<cuuint64_t>(H) * kHeadDim * e,
+                           static_cast<cuuint64_t>(S) * H * kHeadDim * e};
+  cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(kTile), 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 __global__ void wait_timeout_probe_kernel(uint64_t timeout_ns) {
   __shared__ uint64_t bar;
   __shared__ int abort_flag;
@@ -527,11 +637,19 @@ __global__ void wait_timeout_probe_kernel(uint64_t timeout_ns) {
 cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream) {
   const uint64_t BH = static_cast<uint64_t>(a.B) * a.H;
   CUtensorMap tmQ, tmK, tmV;
-  if (!encode_map(&tmQ, a.q_codes, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, kHeadDim, a.Sq_pad, BH, 64, 128) ||
+  const bool qmap_ok = a.q_bf16 != nullptr
+                           ? encode_map_bshd(&tmQ, a.q_bf16, a.B, a.Sq, a.H)
+                           : encode_map(&tmQ, a.q_codes, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, kHeadDim, a.Sq_pad, BH,
+                                        64, 128);
+  if (!qmap_ok ||
       !encode_map(&tmK, a.k_codes, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, kHeadDim, a.Skv_pad, BH, 64, kKV) ||
       !encode_map(&tmV, a.vt, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.Skv_pad, kHeadDim, BH, 128, 128))
     return cudaErrorInvalidValue;
   Params p;
+  p.fuse_q = a.q_bf16 != nullptr;
+  p.q_dump = a.q_dump;
+  p.q_scale_dump = a.q_scale_dump;
+  p.Sq_pad = a.Sq_pad;
   p.q_scale = a.q_scale;
   p.k_scale = a.k_scale;
   p.v_scale = a.v_scale;

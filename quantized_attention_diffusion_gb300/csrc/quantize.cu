@@ -72,7 +72,7 @@ struct CodeStore<__half> {
 template <typename CodeT>
 __global__ void __launch_bounds__(256) qk_quantize_kernel(QKQuantArgs<CodeT> a) {
   __shared__ float warp_max[8];
-  const int tensor = blockIdx.y;
+  const int tensor = blockIdx.y + a.first;
   const uint16_t* __restrict__ x = tensor == 0 ? a.q : a.k;
   CodeT* __restrict__ codes = tensor == 0 ? a.q_codes : a.k_codes;
   float* __restrict__ scale = tensor == 0 ? a.q_scale : a.k_scale;
@@ -243,9 +243,9 @@ __global__ void __launch_bounds__(256) widen_codes_kernel(const int8_t* __restri
 
 template <typename CodeT>
 cudaError_t launch_qk_quantize(const QKQuantArgs<CodeT>& a, cudaStream_t stream) {
-  const long long blocks = static_cast<long long>(a.BH) * (std::max(a.S_pad[0], a.S_pad[1]) / 32);
+  const long long blocks = static_cast<long long>(a.BH) * (std::max(a.first ? 0 : a.S_pad[0], a.S_pad[1]) / 32);
   const long long ctas = (blocks + 1) / 2;
-  qk_quantize_kernel<CodeT><<<dim3(static_cast<unsigned>(ctas), 2), 256, 0, stream>>>(a);
+  qk_quantize_kernel<CodeT><<<dim3(static_cast<unsigned>(ctas), 2 - a.first), 256, 0, stream>>>(a);
   return cudaGetLastError();
 }
 template cudaError_t launch_qk_quantize<int8_t>(const QKQuantArgs<int8_t>&, cudaStream_t);

@@ -123,8 +123,12 @@ cudaError_t pool_alloc(void** ptr, size_t bytes, cudaStream_t stream) {
 
 uint64_t timeout_ns() { return g_timeout_ns.load(std::memory_order_relaxed); }
 
+// Quantise Q, K and V, then attend.  With fuse_q, only K and V are quantised
+// here and the attention kernel quantises Q itself (q_dump / q_scale_dump
+// then receive its codes and scales, if given).
 sage_status run_fused(const void* q, const void* k, const void* v, void* out, int B, int Sq, int Sk,
-                      int H, float softmax_scale, void* ws, cudaStream_t st, float* lse = nullptr) {
+                      int H, float softmax_scale, void* ws, cudaStream_t st, float* lse = nullptr,
+                      bool fuse_q = false, int8_t* q_dump = nullptr, float* q_scale_dump = nullptr) {
   const WsLayout w = ws_layout(B, Sq, Sk, H);
   QKQuantArgs<__half> qa;
   qa.q = static_cast<const uint16_t*>(q);
@@ -136,16 +140,20 @@ sage_status run_fused(const void* q, const void* k, const void* v, void* out, in
   qa.BH = B * H;
   qa.H = H;
   qa.set_lengths(Sq, Sk);
+  qa.first = fuse_q ? 1 : 0;
   cudaError_t e = launch_qk_quantize<__half>(qa, st);
   if (e != cudaSuccess) return cuda_fail(e, "Q/K quantisation launch");
   e = launch_v_quantize(static_cast<const uint16_t*>(v), B, Sk, H, padded_len(Sk), at<uint32_t>(ws, w.vamax),
                         at<uint8_t>(ws, w.vt), at<float>(ws, w.vs), st);
   if (e != cudaSuccess) return cuda_fail(e, "V quantisation launch");
   AttnArgs aa;
-  aa.q_codes = qa.q_codes;
+  aa.q_bf16 = fuse_q ? static_cast<const uint16_t*>(q) : nullptr;
+  aa.q_dump = q_dump;
+  aa.q_scale_dump = q_scale_dump;
+  aa.q_codes = fuse_q ? nullptr : qa.q_codes;
   aa.k_codes = qa.k_codes;
   aa.vt = at<uint8_t>(ws, w.vt);
-  aa.q_scale = qa.q_scale;
+  aa.q_scale = fuse_q ? nullptr : qa.q_scale;
   aa.k_scale = qa.k_scale;
   aa.v_scale = at<float>(ws, w.vs);
   aa.out = static_cast<uint16_t*>(out);
@@ -181,6 +189,9 @@ sage_status run_quantized(const int8_t* q_i8, const float* q_scale, const int8_t
   if (e == cudaSuccess) e = launch_widen_codes(k_i8, at<__half>(ws, w.k16), n, st);
   if (e != cudaSuccess) return cuda_fail(e, "code widening launch");
   AttnArgs aa;
+  aa.q_bf16 = nullptr;
+  aa.q_dump = nullptr;
+  aa.q_scale_dump = nullptr;
   aa.q_codes = at<__half>(ws, w.q16);
   aa.k_codes = at<__half>(ws, w.k16);
   aa.vt = vt;
@@ -368,6 +379,41 @@ sage_status sage_debug_qk_int32(const int8_t* q_i8, const float* q_scale, const 
   if (s != SAGE_OK) return s;
   return run_quantized(q_i8, q_scale, k_i8, k_scale, vt_fp8, v_scale, out, s_out, B, S, H, softmax_scale,
                        workspace, static_cast<cudaStream_t>(stream));
+}
+
+sage_status sage_attn_fwd_fused_q(const void* q, const void* k, const void* v, void* out, int B, int S,
+                                  int H, int D, float softmax_scale, void* stream) {
+  sage_status s = check_shape(B, S, H, D);
+  if (s == SAGE_OK) s = check_scale(softmax_scale);
+  if (s == SAGE_OK) s = check_ptrs({{q, "q"}, {k, "k"}, {v, "v"}, {out, "out"}});
+  if (s != SAGE_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  void* ws = nullptr;
+  cudaError_t e = pool_alloc(&ws, ws_layout(B, S, S, H).total, st);
+  if (e != cudaSuccess) return fail(SAGE_ERR_NO_MEMORY, "workspace allocation failed: %s", cudaGetErrorString(e));
+  s = run_fused(q, k, v, out, B, S, S, H, softmax_scale, ws, st, nullptr, true);
+  e = cudaFreeAsync(ws, st);
+  if (s != SAGE_OK) return s;
+  if (e != cudaSuccess) return cuda_fail(e, "workspace release");
+  return SAGE_OK;
+}
+
+sage_status sage_debug_fused_q(const void* q, const void* k, const void* v, void* out, int B, int S, int H,
+                               int D, float softmax_scale, int8_t* q_i8, float* q_scale, void* stream) {
+  sage_status s = check_shape(B, S, H, D);
+  if (s == SAGE_OK) s = check_scale(softmax_scale);
+  if (s == SAGE_OK)
+    s = check_ptrs({{q, "q"}, {k, "k"}, {v, "v"}, {out, "out"}, {q_i8, "q_i8"}, {q_scale, "q_scale"}});
+  if (s != SAGE_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  void* ws = nullptr;
+  cudaError_t e = pool_alloc(&ws, ws_layout(B, S, S, H).total, st);
+  if (e != cudaSuccess) return fail(SAGE_ERR_NO_MEMORY, "workspace allocation failed: %s", cudaGetErrorString(e));
+  s = run_fused(q, k, v, out, B, S, S, H, softmax_scale, ws, st, nullptr, true, q_i8, q_scale);
+  e = cudaFreeAsync(ws, st);
+  if (s != SAGE_OK) return s;
+  if (e != cudaSuccess) return cuda_fail(e, "workspace release");
+  return SAGE_OK;
 }
 
 sage_status sage_debug_wait_timeout(uint64_t ns, void* stream) {

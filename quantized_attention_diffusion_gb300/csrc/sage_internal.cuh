@@ -30,6 +30,7 @@ struct QKQuantArgs {
   float* k_scale;
   int BH, H;
   int S[2], S_pad[2], nb[2];   // per tensor: [0] Q, [1] K (cross-attention: they differ)
+  int first = 0;               // 1: quantise K only (Q is quantised inside the attention kernel)
   void set_lengths(int Sq, int Sk) {
     S[0] = Sq; S_pad[0] = padded_len(Sq); nb[0] = num_blocks(Sq);
     S[1] = Sk; S_pad[1] = padded_len(Sk); nb[1] = num_blocks(Sk);
@@ -46,6 +47,10 @@ cudaError_t launch_v_quantize(const uint16_t* v, int B, int S, int H, int S_pad,
 cudaError_t launch_widen_codes(const int8_t* src, __half* dst, size_t n, cudaStream_t stream);
 
 struct AttnArgs {
+  const uint16_t* q_bf16;   // if set: bf16 Q [B, Sq, H, 128], quantised inside the attention kernel
+                            // (q_codes and q_scale are then not read)
+  int8_t* q_dump;           // optional (with q_bf16): the kernel's Q codes, int8 [B, H, Sq_pad, 128]
+  float* q_scale_dump;      // optional (with q_bf16): its Q block scales [B, H, nbq]
   const __half* q_codes;    // integer-valued fp16 codes [B, H, S_pad, 128]
   const __half* k_codes;
   const uint8_t* vt;        // e4m3 V^T [B, H, 128, S_pad]

@@ -34,6 +34,7 @@ EXPORTED = (
     "sage_debug_wait_timeout", "sage_sync_status", "sage_set_wait_timeout_ns",
     "sage_last_error", "sage_status_string", "sage_set_attention_events",
     "sage_quantize_qkv_noalloc", "sage_attn_fwd_lse", "sage_attn_fwd_cross",
+    "sage_debug_fused_q", "sage_attn_fwd_fused_q",
 )
 
 
@@ -71,6 +72,8 @@ def load_library(path: str = LIB_PATH):
             "sage_attn_fwd_ws": (S, [P, P, P, P, I, I, I, I, F, P, Z, P]),
             "sage_attn_fwd_lse": (S, [P, P, P, P, P, I, I, I, I, F, P]),
             "sage_attn_fwd_cross": (S, [P, P, P, P, P, I, I, I, I, I, F, P]),
+            "sage_debug_fused_q": (S, [P, P, P, P, I, I, I, I, F, P, P, P]),
+            "sage_attn_fwd_fused_q": (S, [P, P, P, P, I, I, I, I, F, P]),
             "sage_attn_fwd_quantized": (S, [P, P, P, P, P, P, P, I, I, I, I, F, P, Z, P]),
             "sage_debug_qk_int32": (S, [P, P, P, P, P, P, P, P, I, I, I, I, F, P, Z, P]),
             "sage_debug_wait_timeout": (S, [ctypes.c_uint64, P]),
@@ -131,11 +134,13 @@ def workspace_bytes(B: int, S: int, H: int, D: int = HEAD_DIM) -> int:
     return int(load_library().sage_workspace_bytes(B, S, H, D))
 
 
-def attn_fwd(q, k, v, softmax_scale: float | None = None, out=None, workspace=None):
+def attn_fwd(q, k, v, softmax_scale: float | None = None, out=None, workspace=None, fused_q=False):
     """Quantized attention forward: bf16 [B, S, H, 128] -> bf16 [B, S, H, 128].
 
     ``workspace`` (optional uint8 CUDA tensor of >= workspace_bytes) selects
     sage_attn_fwd_ws; otherwise the library's stream-ordered pool is used.
+    ``fused_q`` selects sage_attn_fwd_fused_q (Q quantised in the attention
+    kernel; same result).
     """
     lib = load_library()
     B, S, H, D = _check_qkv(q, k, v)
@@ -145,7 +150,10 @@ def attn_fwd(q, k, v, softmax_scale: float | None = None, out=None, workspace=No
         out = torch.empty_like(q)
     with torch.cuda.device(q.device):
         st = _stream(q.device)
-        if workspace is None:
+        if fused_q:
+            _check(lib.sage_attn_fwd_fused_q(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, S, H, D,
+                                             float(softmax_scale), st))
+        elif workspace is None:
             _check(lib.sage_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, S, H, D,
                                      float(softmax_scale), st))
         else:
@@ -209,6 +217,24 @@ def attn_fwd_cross(q, k, v, softmax_scale: float | None = None, out=None, lse=No
                                        _ptr(lse) if lse is not None else None, B, Sq, Skv, H, D,
                                        float(softmax_scale), _stream(q.device)))
     return (out, lse) if lse is not None else out
+
+
+def debug_fused_q(q, k, v, softmax_scale: float | None = None):
+    """Run sage_attn_fwd's path and return (out, q_i8 [B,H,S_pad,D],
+    q_scale [B,H,nb]): the Q codes and scales the attention kernel computed."""
+    lib = load_library()
+    B, S, H, D = _check_qkv(q, k, v)
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(D)
+    Sp = padded_len(S)
+    nb = (S + 31) // 32
+    out = torch.empty_like(q)
+    q_i8 = torch.zeros((B, H, Sp, D), dtype=torch.int8, device=q.device)
+    q_scale = torch.zeros((B, H, nb), dtype=torch.float32, device=q.device)
+    with torch.cuda.device(q.device):
+        _check(lib.sage_debug_fused_q(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, S, H, D, float(softmax_scale),
+                                      _ptr(q_i8), _ptr(q_scale), _stream(q.device)))
+    return out, q_i8, q_scale
 
 
 def quantize_qkv(q, k, v, out=None, noalloc=False):
