@@ -55,6 +55,8 @@ def parse_args():
                     help="time sage_attn_fwd_lse (also writes the per-row log-sum-exp)")
     ap.add_argument("--fused-q", action="store_true",
                     help="time sage_attn_fwd_fused_q (Q quantised inside the attention kernel)")
+    ap.add_argument("--smooth-k", action="store_true",
+                    help="time sage_attn_fwd_smooth_k (K loses its per-channel mean before quantisation)")
     ap.add_argument("--no-e2e", action="store_true",
                     help="skip the host-buffer leg (for short profiling runs; the line then has no e2e figure)")
     return ap.parse_args()
@@ -256,7 +258,7 @@ def run_ours(args, group, local):
         elif args.lse:
             qad.attn_fwd_lse(qq, kk, vv, w.softmax_scale, out=oo, lse=ll)
         else:
-            qad.attn_fwd(qq, kk, vv, w.softmax_scale, out=oo, fused_q=args.fused_q)
+            qad.attn_fwd(qq, kk, vv, w.softmax_scale, out=oo, fused_q=args.fused_q, smooth_k=args.smooth_k)
 
     for _ in range(W):
         step(q, k, v, out, lse)
@@ -369,7 +371,8 @@ def run_ours(args, group, local):
         "config": {
             "workload": w.name, "B": w.B, "S": w.S, "Skv": w.skv, "H": w.H, "D": w.D, "recipe": w.recipe,
             "seed": w.seed, "softmax_scale": w.softmax_scale, "path": ("sage_attn_fwd_cross" if w.Skv is not None else "sage_attn_fwd_lse" if args.lse
-                     else "sage_attn_fwd_fused_q" if args.fused_q else "sage_attn_fwd") + (" (quantise + attention + LSE)" if args.lse
+                     else "sage_attn_fwd_fused_q" if args.fused_q
+                     else "sage_attn_fwd_smooth_k" if args.smooth_k else "sage_attn_fwd") + (" (quantise + attention + LSE)" if args.lse
                                                else " (quantise + attention)"),
             "l2": f"inputs larger than L2 ({in_bytes / 1e6:.0f} MB read per step, L2 129 MB)",
             "parallelism": "replicas" if group.world > 1 else "single GPU",

@@ -171,6 +171,29 @@ sage_status sage_attn_fwd_cross(const void* q, const void* k, const void* v, voi
                                 int Sq, int Skv, int H, int D, float softmax_scale, void* stream);
 
 /*
+ * sage_quantize_qkv_smooth_k -- sage_quantize_qkv with K smoothing: before K
+ * is quantised, each (batch, head, channel) loses its mean over the S
+ * tokens.  Passage: InvokeAI PR #9657, "Summary" / "How it works"
+ * (SageAttention's smooth_k; softmax-invariant, since every score of a query
+ * row moves by the same q . mean).
+ *   k_mean  out: fp32 [B, H, D]: fp32(sum_s k / S), the sum exact in double
+ *   k_i8, k_scale: codes and block scales of fp32(k - mean); other outputs,
+ *   layouts and errors as sage_quantize_qkv.
+ */
+sage_status sage_quantize_qkv_smooth_k(const void* q, const void* k, const void* v, int B, int S, int H, int D,
+                                       int8_t* q_i8, float* q_scale, int8_t* k_i8, float* k_scale, uint8_t* vt_fp8,
+                                       float* v_scale, float* k_mean, void* stream);
+
+/*
+ * sage_attn_fwd_smooth_k -- sage_attn_fwd with K smoothing (as
+ * sage_quantize_qkv_smooth_k) before the attention step.  The pages measure
+ * it helping typical heads and hurting outlier heads, so it is opt-in.
+ * Arguments and errors as sage_attn_fwd.
+ */
+sage_status sage_attn_fwd_smooth_k(const void* q, const void* k, const void* v, void* out, int B, int S, int H,
+                                   int D, float softmax_scale, void* stream);
+
+/*
  * sage_attn_fwd_fused_q -- sage_attn_fwd with Q quantised inside the
  * attention kernel, as the pages' kernel does (issue #15014, contract
  * bullet "quantized per 32-row block ... inside the kernel"): the kernel

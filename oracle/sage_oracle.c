@@ -58,8 +58,9 @@
  *  R15 (K smoothing, optional) before K is quantised, each (batch, head,
  *      channel d) of K loses its mean over the S tokens: mean_d =
  *      fp32(sum_s k_sd / S), the sum taken in double (exact for bf16 inputs
- *      whose magnitudes span fewer than 45 - log2 S binary orders) and the
- *      division in double, rounded once; k'_sd = fl32(k_sd - mean_d); k' is
+ *      whose magnitudes span fewer than 45 - log2 S binary orders: any exact
+ *      method gives the same mean) and the division in double, rounded once;
+ *      k'_sd = fl32(k_sd - mean_d); k' is
  *      then quantised as R1/R2.  Every score of a query row moves by the
  *      same q . mean, so the softmax is unchanged in exact arithmetic.
  *  R14 (cross-attention) Q may have Sq rows and K, V S != Sq rows: each is

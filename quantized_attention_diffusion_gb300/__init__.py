@@ -8,4 +8,5 @@ output ``[B, S, H, 128]``.  The work runs in ``libsage.so`` (C ABI in
 from .sage import (EXPORTED, HEAD_DIM, LIB_PATH, SageError, attn_fwd, attn_fwd_cross, attn_fwd_lse,  # noqa: F401
                    attn_fwd_quantized,
                    debug_fused_q, debug_qk_int32, debug_wait_timeout, load_library, padded_len, quantize_qkv,
+                   quantize_qkv_smooth_k,
                    set_attention_events, set_wait_timeout_ns, sync_status, workspace_bytes)

@@ -231,7 +231,7 @@ __device__ __forceinline__ float quantize_q_rows(uint8_t* tile, int r, int bh, i
   return sc;
 }
 
-template <bool kDumpS>
+template <bool kDumpS, bool kFuseQ>
 __global__ void __launch_bounds__(kThreads, 1)
     sage_attn_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const Params p) {
@@ -301,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       mbar_arrive_expect_tx(&bars.q_full, 2 * kQTileBytes);
       for (int t = 0; t < 2; ++t) {
-        if (p.fuse_q) {   // bf16 [B, S, H, 128]: box of 64 channels x 128 tokens of one (b, h)
+        if constexpr (kFuseQ) {   // bf16 [B, S, H, 128]: box of 64 channels x 128 tokens of one (b, h)
           const int b = bh / p.H, h = bh % p.H;
           tma_load_4d(sQ + t * kQTileBytes, &tmQ, &bars.q_full, 0, h, q_row0 + t * kTile, b);
           tma_load_4d(sQ + t * kQTileBytes + kQHalf, &tmQ, &bars.q_full, 64, h, q_row0 + t * kTile, b);
@@ -336,7 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t idesc = make_idesc_f32acc(128, kKV, 0, 0);   // F16 x F16 -> F32
       const uint32_t q_lo = sw128_desc_lo(smem_addr(sQ)), k_lo = sw128_desc_lo(smem_addr(sK));
       // Q codes: straight from TMA, or after the softmax warps quantised them.
-      if (wait_bar(p.fuse_q ? &bars.q_ready : &bars.q_full, 0, abort_v, p.timeout_ns)) {
+      if (wait_bar(kFuseQ ? &bars.q_ready : &bars.q_full, 0, abort_v, p.timeout_ns)) {
         for (int j = 0; j < p.n_kv; ++j) {
           const int s = j % kStages;
           if (!wait_bar(&bars.k_full[s], (j / kStages) & 1, abort_v, p.timeout_ns)) break;
@@ -407,7 +407,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float* ksc = p.k_scale + static_cast<size_t>(bh) * p.nbk;
     float sq = 0.0f;
     bool ok = true;
-    if (p.fuse_q) {
+    if constexpr (kFuseQ) {
       // Quantise this warp's own 32 rows of Q (one K-block-sized Q block, the
       // rows its softmax serves) in place: bf16 in, integer-valued fp16 out.
       ok = __all_sync(0xFFFFFFFFu, wait_bar(&bars.q_full, 0, abort_v, p.timeout_ns));
@@ -668,17 +668,17 @@ cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream) {
   const uint64_t grid = BH * static_cast<uint64_t>(p.n_pairs);
   if (grid > 0x7FFFFFFFull) return cudaErrorInvalidConfiguration;
   cudaError_t e;
-  if (a.s_dump) {
-    e = cudaFuncSetAttribute(sage_attn_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSmemDynamic);
-    if (e != cudaSuccess) return e;
-    sage_attn_kernel<true><<<static_cast<unsigned>(grid), kThreads, kSmemDynamic, stream>>>(tmQ, tmK, tmV, p);
-  } else {
-    e = cudaFuncSetAttribute(sage_attn_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSmemDynamic);
-    if (e != cudaSuccess) return e;
-    sage_attn_kernel<false><<<static_cast<unsigned>(grid), kThreads, kSmemDynamic, stream>>>(tmQ, tmK, tmV, p);
-  }
+  auto go = [&](auto kernel) {
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemDynamic);
+    if (e == cudaSuccess) kernel<<<static_cast<unsigned>(grid), kThreads, kSmemDynamic, stream>>>(tmQ, tmK, tmV, p);
+  };
+  if (a.s_dump)
+    go(sage_attn_kernel<true, false>);
+  else if (p.fuse_q)
+    go(sage_attn_kernel<false, true>);
+  else
+    go(sage_attn_kernel<false, false>);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -69,7 +69,7 @@ struct CodeStore<__half> {
 // lanes 0-15 the even token of a pair, lanes 16-31 the odd one, lane%16 owns
 // channels 8*(lane%16) .. +7.  The block max is a warp shuffle then a
 // shared-memory max over the four warps.  grid.y selects Q (0) or K (1).
-template <typename CodeT>
+template <typename CodeT, bool kSmooth>
 __global__ void __launch_bounds__(256) qk_quantize_kernel(QKQuantArgs<CodeT> a) {
   __shared__ float warp_max[8];
   const int tensor = blockIdx.y + a.first;
@@ -88,6 +88,15 @@ __global__ void __launch_bounds__(256) qk_quantize_kernel(QKQuantArgs<CodeT> a) 
   const int b = bh / a.H, h = bh % a.H;
   const int half = lane >> 4;
   const int c8 = (lane & 15) * 8;
+  // K smoothing: subtract the channel means before quantising.
+  float mu[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  const bool smooth = kSmooth && tensor == 1;
+  if (smooth && active) {
+    const float4* m4 = reinterpret_cast<const float4*>(a.k_mean + static_cast<size_t>(bh) * kHeadDim + c8);
+    const float4 m0 = m4[0], m1 = m4[1];
+    mu[0] = m0.x; mu[1] = m0.y; mu[2] = m0.z; mu[3] = m0.w;
+    mu[4] = m1.x; mu[5] = m1.y; mu[6] = m1.z; mu[7] = m1.w;
+  }
   const int tok0 = blk * 32 + w4 * 8 + half;   // this lane's first token; then +2, +4, +6
   const size_t tok_stride = static_cast<size_t>(a.H) * kHeadDim;
   const uint16_t* src = x + (static_cast<size_t>(b) * S * a.H + h) * kHeadDim + c8;
@@ -97,13 +106,20 @@ __global__ void __launch_bounds__(256) qk_quantize_kernel(QKQuantArgs<CodeT> a) 
 #pragma unroll
   for (int it = 0; it < 4; ++it) {
     const int s = tok0 + 2 * it;
-    raw[it] = (active && s < S)
-                  ? __ldcs(reinterpret_cast<const uint4*>(src + static_cast<size_t>(s) * tok_stride))
-                  : make_uint4(0, 0, 0, 0);
+    const bool valid = active && s < S;
+    raw[it] = valid ? __ldcs(reinterpret_cast<const uint4*>(src + static_cast<size_t>(s) * tok_stride))
+                    : make_uint4(0, 0, 0, 0);
     const uint32_t w[4] = {raw[it].x, raw[it].y, raw[it].z, raw[it].w};
+    if (smooth) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
-      amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w[i])), fabsf(bf16_hi(w[i]))));
+      for (int i = 0; i < 4; ++i)
+        if (valid)
+          amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w[i]) - mu[2 * i]), fabsf(bf16_hi(w[i]) - mu[2 * i + 1])));
+    } else {
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w[i])), fabsf(bf16_hi(w[i]))));
+    }
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
@@ -120,10 +136,11 @@ __global__ void __launch_bounds__(256) qk_quantize_kernel(QKQuantArgs<CodeT> a) 
   for (int it = 0; it < 4; ++it) {
     const uint32_t w[4] = {raw[it].x, raw[it].y, raw[it].z, raw[it].w};
     int c[8];
+    const bool valid = tok0 + 2 * it < S;   // rows past the end stay 0 (no -mean)
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      c[2 * i] = qk_code(bf16_lo(w[i]), sc);
-      c[2 * i + 1] = qk_code(bf16_hi(w[i]), sc);
+      c[2 * i] = qk_code(smooth && valid ? bf16_lo(w[i]) - mu[2 * i] : bf16_lo(w[i]), sc);
+      c[2 * i + 1] = qk_code(smooth && valid ? bf16_hi(w[i]) - mu[2 * i + 1] : bf16_hi(w[i]), sc);
     }
     CodeStore<CodeT>::store(dst + static_cast<size_t>(2 * it) * kHeadDim, c);
   }
@@ -162,6 +179,63 @@ __global__ void __launch_bounds__(256) v_amax_kernel(const uint16_t* __restrict_
 #pragma unroll
     for (int i = 1; i < 16; ++i) mm = fmaxf(mm, part[i][t]);
     atomicMax(amax_bits + static_cast<size_t>(bh) * kHeadDim + t, __float_as_uint(mm));
+  }
+}
+
+// A bf16 value times 2^40 as a 64-bit integer: exact for |x| in [2^-33, 2^22)
+// (8 significant bits, the lowest at or above 2^-40) and for 0; smaller
+// magnitudes are truncated, larger ones saturate.  A channel's sum stays
+// exact while its magnitude is below 2^23, and converts to double exactly
+// below 2^13 (bf16 activations of a few units sum far below that).
+__device__ __forceinline__ long long bf16_fixed40(uint32_t h) {
+  const uint32_t e = (h >> 7) & 0xFFu;
+  const long long m = static_cast<long long>((h & 0x7Fu) | (e ? 0x80u : 0u));
+  const int sh = static_cast<int>(e ? e : 1u) - 127 - 7 + 40;
+  long long v = sh >= 0 ? (sh < 55 ? (m << sh) : (255LL << 54)) : (sh > -8 ? (m >> -sh) : 0LL);
+  return (h & 0x8000u) ? -v : v;
+}
+
+// Per-channel sums of K over one 256-token slice of one (batch, head), in
+// 64-bit fixed point (2^-40): integer additions, so the merged result does not
+// depend on the order of the slices, and it equals the exact sum for the
+// magnitudes bf16_fixed40 keeps exactly.
+__global__ void __launch_bounds__(256) k_sum_kernel(const uint16_t* __restrict__ k, int S, int H,
+                                                    unsigned long long* __restrict__ sums) {
+  __shared__ long long part[16][kHeadDim];
+  const int bh = blockIdx.y, b = bh / H, h = bh % H;
+  const int t = threadIdx.x, c8 = (t & 15) * 8, r = t >> 4;
+  const int s0 = blockIdx.x * kVRowsPerCta;
+  const int s1 = min(S, s0 + kVRowsPerCta);
+  const size_t tok_stride = static_cast<size_t>(H) * kHeadDim;
+  const uint16_t* src = k + (static_cast<size_t>(b) * S * H + h) * kHeadDim + c8;
+  long long m[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  for (int s = s0 + r; s < s1; s += 16) {
+    const uint4 q = __ldg(reinterpret_cast<const uint4*>(src + static_cast<size_t>(s) * tok_stride));
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      m[2 * i] += bf16_fixed40(w[i] & 0xFFFFu);
+      m[2 * i + 1] += bf16_fixed40(w[i] >> 16);
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) part[r][c8 + i] = m[i];
+  __syncthreads();
+  if (t < kHeadDim) {
+    long long mm = part[0][t];
+#pragma unroll
+    for (int i = 1; i < 16; ++i) mm += part[i][t];
+    atomicAdd(sums + static_cast<size_t>(bh) * kHeadDim + t, static_cast<unsigned long long>(mm));
+  }
+}
+
+// mean = fp32(sum / S) per (batch, head, channel): the fixed-point sum is
+// converted to double (exact below 2^53 units of 2^-40) and divided once.
+__global__ void k_mean_kernel(const unsigned long long* __restrict__ sums, int S, int n, float* __restrict__ mean) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) {
+    const double sum = static_cast<double>(static_cast<long long>(sums[i])) * 0x1p-40;
+    mean[i] = static_cast<float>(sum / static_cast<double>(S));
   }
 }
 
@@ -245,7 +319,11 @@ template <typename CodeT>
 cudaError_t launch_qk_quantize(const QKQuantArgs<CodeT>& a, cudaStream_t stream) {
   const long long blocks = static_cast<long long>(a.BH) * (std::max(a.first ? 0 : a.S_pad[0], a.S_pad[1]) / 32);
   const long long ctas = (blocks + 1) / 2;
-  qk_quantize_kernel<CodeT><<<dim3(static_cast<unsigned>(ctas), 2 - a.first), 256, 0, stream>>>(a);
+  const dim3 grid(static_cast<unsigned>(ctas), 2 - a.first);
+  if (a.k_mean != nullptr)
+    qk_quantize_kernel<CodeT, true><<<grid, 256, 0, stream>>>(a);
+  else
+    qk_quantize_kernel<CodeT, false><<<grid, 256, 0, stream>>>(a);
   return cudaGetLastError();
 }
 template cudaError_t launch_qk_quantize<int8_t>(const QKQuantArgs<int8_t>&, cudaStream_t);
@@ -260,6 +338,19 @@ cudaError_t launch_v_quantize(const uint16_t* v, int B, int S, int H, int S_pad,
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   v_encode_kernel<<<dim3(S_pad / 128, BH), 256, 0, stream>>>(v, S, H, S_pad, amax_bits, vt, v_scale);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_k_channel_means(const uint16_t* k, int B, int S, int H, unsigned long long* sums, float* mean,
+                                   cudaStream_t stream) {
+  const int BH = B * H;
+  cudaError_t e = cudaMemsetAsync(sums, 0, static_cast<size_t>(BH) * kHeadDim * sizeof(unsigned long long), stream);
+  if (e != cudaSuccess) return e;
+  k_sum_kernel<<<dim3((S + kVRowsPerCta - 1) / kVRowsPerCta, BH), 256, 0, stream>>>(k, S, H, sums);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int n = BH * kHeadDim;
+  k_mean_kernel<<<(n + 255) / 256, 256, 0, stream>>>(sums, S, n, mean);
   return cudaGetLastError();
 }
 

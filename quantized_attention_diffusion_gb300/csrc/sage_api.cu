@@ -64,7 +64,7 @@ sage_status check_ptrs(std::initializer_list<std::pair<const void*, const char*>
 
 // Workspace layout (all offsets 256-byte aligned).
 struct WsLayout {
-  size_t q16, k16, vt, qs, ks, vs, vamax, total;
+  size_t q16, k16, vt, qs, ks, vs, vamax, ksum, kmean, total;
 };
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
@@ -82,6 +82,8 @@ WsLayout ws_layout(int B, int Sq, int Sk, int H) {
   w.ks = off; off += align256(BH * nbk * sizeof(float));
   w.vs = off; off += align256(BH * kHeadDim * sizeof(float));
   w.vamax = off; off += align256(BH * kHeadDim * sizeof(uint32_t));
+  w.ksum = off; off += align256(BH * kHeadDim * sizeof(unsigned long long));
+  w.kmean = off; off += align256(BH * kHeadDim * sizeof(float));
   w.total = off;
   return w;
 }
@@ -128,8 +130,14 @@ uint64_t timeout_ns() { return g_timeout_ns.load(std::memory_order_relaxed); }
 // then receive its codes and scales, if given).
 sage_status run_fused(const void* q, const void* k, const void* v, void* out, int B, int Sq, int Sk,
                       int H, float softmax_scale, void* ws, cudaStream_t st, float* lse = nullptr,
-                      bool fuse_q = false, int8_t* q_dump = nullptr, float* q_scale_dump = nullptr) {
+                      bool fuse_q = false, int8_t* q_dump = nullptr, float* q_scale_dump = nullptr,
+                      bool smooth_k = false) {
   const WsLayout w = ws_layout(B, Sq, Sk, H);
+  if (smooth_k) {
+    cudaError_t e0 = launch_k_channel_means(static_cast<const uint16_t*>(k), B, Sk, H, at<unsigned long long>(ws, w.ksum),
+                                            at<float>(ws, w.kmean), st);
+    if (e0 != cudaSuccess) return cuda_fail(e0, "K channel means launch");
+  }
   QKQuantArgs<__half> qa;
   qa.q = static_cast<const uint16_t*>(q);
   qa.k = static_cast<const uint16_t*>(k);
@@ -141,6 +149,7 @@ sage_status run_fused(const void* q, const void* k, const void* v, void* out, in
   qa.H = H;
   qa.set_lengths(Sq, Sk);
   qa.first = fuse_q ? 1 : 0;
+  qa.k_mean = smooth_k ? at<float>(ws, w.kmean) : nullptr;
   cudaError_t e = launch_qk_quantize<__half>(qa, st);
   if (e != cudaSuccess) return cuda_fail(e, "Q/K quantisation launch");
   e = launch_v_quantize(static_cast<const uint16_t*>(v), B, Sk, H, padded_len(Sk), at<uint32_t>(ws, w.vamax),
@@ -276,6 +285,62 @@ sage_status sage_quantize_qkv(const void* q, const void* k, const void* v, int B
   cudaError_t e2 = cudaFreeAsync(scratch, st);
   if (e != cudaSuccess) return cuda_fail(e, "V quantisation launch");
   if (e2 != cudaSuccess) return cuda_fail(e2, "scratch release");
+  return SAGE_OK;
+}
+
+sage_status sage_quantize_qkv_smooth_k(const void* q, const void* k, const void* v, int B, int S, int H, int D,
+                                       int8_t* q_i8, float* q_scale, int8_t* k_i8, float* k_scale, uint8_t* vt_fp8,
+                                       float* v_scale, float* k_mean, void* stream) {
+  sage_status s = check_shape(B, S, H, D);
+  if (s == SAGE_OK)
+    s = check_ptrs({{q, "q"}, {k, "k"}, {v, "v"}, {q_i8, "q_i8"}, {q_scale, "q_scale"}, {k_i8, "k_i8"},
+                    {k_scale, "k_scale"}, {vt_fp8, "vt_fp8"}, {v_scale, "v_scale"}, {k_mean, "k_mean"}});
+  if (s != SAGE_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t BH = static_cast<size_t>(B) * H;
+  const size_t sum_bytes = align256(BH * kHeadDim * sizeof(unsigned long long));
+  void* scratch = nullptr;
+  cudaError_t e = pool_alloc(&scratch, sum_bytes + BH * kHeadDim * sizeof(uint32_t), st);
+  if (e != cudaSuccess) return fail(SAGE_ERR_NO_MEMORY, "scratch allocation failed: %s", cudaGetErrorString(e));
+  unsigned long long* sums = static_cast<unsigned long long*>(scratch);
+  e = launch_k_channel_means(static_cast<const uint16_t*>(k), B, S, H, sums, k_mean, st);
+  if (e == cudaSuccess) {
+    QKQuantArgs<int8_t> qa;
+    qa.q = static_cast<const uint16_t*>(q);
+    qa.k = static_cast<const uint16_t*>(k);
+    qa.q_codes = q_i8;
+    qa.k_codes = k_i8;
+    qa.q_scale = q_scale;
+    qa.k_scale = k_scale;
+    qa.BH = B * H;
+    qa.H = H;
+    qa.set_lengths(S, S);
+    qa.k_mean = k_mean;
+    e = launch_qk_quantize<int8_t>(qa, st);
+  }
+  if (e == cudaSuccess)
+    e = launch_v_quantize(static_cast<const uint16_t*>(v), B, S, H, padded_len(S),
+                          at<uint32_t>(scratch, sum_bytes), vt_fp8, v_scale, st);
+  cudaError_t e2 = cudaFreeAsync(scratch, st);
+  if (e != cudaSuccess) return cuda_fail(e, "quantisation launch");
+  if (e2 != cudaSuccess) return cuda_fail(e2, "scratch release");
+  return SAGE_OK;
+}
+
+sage_status sage_attn_fwd_smooth_k(const void* q, const void* k, const void* v, void* out, int B, int S, int H,
+                                   int D, float softmax_scale, void* stream) {
+  sage_status s = check_shape(B, S, H, D);
+  if (s == SAGE_OK) s = check_scale(softmax_scale);
+  if (s == SAGE_OK) s = check_ptrs({{q, "q"}, {k, "k"}, {v, "v"}, {out, "out"}});
+  if (s != SAGE_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  void* ws = nullptr;
+  cudaError_t e = pool_alloc(&ws, ws_layout(B, S, S, H).total, st);
+  if (e != cudaSuccess) return fail(SAGE_ERR_NO_MEMORY, "workspace allocation failed: %s", cudaGetErrorString(e));
+  s = run_fused(q, k, v, out, B, S, S, H, softmax_scale, ws, st, nullptr, false, nullptr, nullptr, true);
+  e = cudaFreeAsync(ws, st);
+  if (s != SAGE_OK) return s;
+  if (e != cudaSuccess) return cuda_fail(e, "workspace release");
   return SAGE_OK;
 }
 

@@ -31,6 +31,7 @@ struct QKQuantArgs {
   int BH, H;
   int S[2], S_pad[2], nb[2];   // per tensor: [0] Q, [1] K (cross-attention: they differ)
   int first = 0;               // 1: quantise K only (Q is quantised inside the attention kernel)
+  const float* k_mean = nullptr;   // K smoothing: per (b, h, d) means of K over its tokens [B*H*128]
   void set_lengths(int Sq, int Sk) {
     S[0] = Sq; S_pad[0] = padded_len(Sq); nb[0] = num_blocks(Sq);
     S[1] = Sk; S_pad[1] = padded_len(Sk); nb[1] = num_blocks(Sk);
@@ -39,6 +40,12 @@ struct QKQuantArgs {
 
 template <typename CodeT>
 cudaError_t launch_qk_quantize(const QKQuantArgs<CodeT>& a, cudaStream_t stream);
+
+// K smoothing: per-channel means of K over its S tokens, mean = fp32(sum / S)
+// with the sum exact (64-bit fixed point, 2^-40, for |k| in [2^-33, 2^23)).
+// sums: [B*H*128] 64-bit scratch (zeroed here); mean: [B*H*128] floats out.
+cudaError_t launch_k_channel_means(const uint16_t* k, int B, int S, int H, unsigned long long* sums, float* mean,
+                                   cudaStream_t stream);
 
 // V channel maxima (amax_bits [B*H*128], zeroed here) then E4M3 V^T codes.
 cudaError_t launch_v_quantize(const uint16_t* v, int B, int S, int H, int S_pad, uint32_t* amax_bits,

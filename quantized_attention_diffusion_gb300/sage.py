@@ -34,7 +34,8 @@ EXPORTED = (
     "sage_debug_wait_timeout", "sage_sync_status", "sage_set_wait_timeout_ns",
     "sage_last_error", "sage_status_string", "sage_set_attention_events",
     "sage_quantize_qkv_noalloc", "sage_attn_fwd_lse", "sage_attn_fwd_cross",
-    "sage_debug_fused_q", "sage_attn_fwd_fused_q",
+    "sage_debug_fused_q", "sage_attn_fwd_fused_q", "sage_quantize_qkv_smooth_k",
+    "sage_attn_fwd_smooth_k",
 )
 
 
@@ -74,6 +75,8 @@ def load_library(path: str = LIB_PATH):
             "sage_attn_fwd_cross": (S, [P, P, P, P, P, I, I, I, I, I, F, P]),
             "sage_debug_fused_q": (S, [P, P, P, P, I, I, I, I, F, P, P, P]),
             "sage_attn_fwd_fused_q": (S, [P, P, P, P, I, I, I, I, F, P]),
+            "sage_quantize_qkv_smooth_k": (S, [P, P, P, I, I, I, I, P, P, P, P, P, P, P, P]),
+            "sage_attn_fwd_smooth_k": (S, [P, P, P, P, I, I, I, I, F, P]),
             "sage_attn_fwd_quantized": (S, [P, P, P, P, P, P, P, I, I, I, I, F, P, Z, P]),
             "sage_debug_qk_int32": (S, [P, P, P, P, P, P, P, P, I, I, I, I, F, P, Z, P]),
             "sage_debug_wait_timeout": (S, [ctypes.c_uint64, P]),
@@ -134,13 +137,15 @@ def workspace_bytes(B: int, S: int, H: int, D: int = HEAD_DIM) -> int:
     return int(load_library().sage_workspace_bytes(B, S, H, D))
 
 
-def attn_fwd(q, k, v, softmax_scale: float | None = None, out=None, workspace=None, fused_q=False):
+def attn_fwd(q, k, v, softmax_scale: float | None = None, out=None, workspace=None, fused_q=False,
+             smooth_k=False):
     """Quantized attention forward: bf16 [B, S, H, 128] -> bf16 [B, S, H, 128].
 
     ``workspace`` (optional uint8 CUDA tensor of >= workspace_bytes) selects
     sage_attn_fwd_ws; otherwise the library's stream-ordered pool is used.
     ``fused_q`` selects sage_attn_fwd_fused_q (Q quantised in the attention
-    kernel; same result).
+    kernel; same result); ``smooth_k`` selects sage_attn_fwd_smooth_k (K loses
+    its per-channel mean before quantisation).
     """
     lib = load_library()
     B, S, H, D = _check_qkv(q, k, v)
@@ -150,7 +155,10 @@ def attn_fwd(q, k, v, softmax_scale: float | None = None, out=None, workspace=No
         out = torch.empty_like(q)
     with torch.cuda.device(q.device):
         st = _stream(q.device)
-        if fused_q:
+        if smooth_k:
+            _check(lib.sage_attn_fwd_smooth_k(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, S, H, D,
+                                              float(softmax_scale), st))
+        elif fused_q:
             _check(lib.sage_attn_fwd_fused_q(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, S, H, D,
                                              float(softmax_scale), st))
         elif workspace is None:
@@ -268,6 +276,28 @@ def quantize_qkv(q, k, v, out=None, noalloc=False):
         _check(fn(_ptr(q), _ptr(k), _ptr(v), B, S, H, D, _ptr(q_i8), _ptr(q_sc),
                   _ptr(k_i8), _ptr(k_sc), _ptr(vt), _ptr(v_sc), _stream(dev)))
     return q_i8, q_sc, k_i8, k_sc, vt, v_sc
+
+
+def quantize_qkv_smooth_k(q, k, v):
+    """sage_quantize_qkv_smooth_k: returns (q_i8, q_scale, k_i8, k_scale,
+    vt_fp8, v_scale, k_mean [B,H,D]) with K smoothed before quantisation."""
+    lib = load_library()
+    B, S, H, D = _check_qkv(q, k, v)
+    Sp = padded_len(S)
+    nb = (S + 31) // 32
+    dev = q.device
+    q_i8 = torch.empty((B, H, Sp, D), dtype=torch.int8, device=dev)
+    k_i8 = torch.empty_like(q_i8)
+    q_sc = torch.empty((B, H, nb), dtype=torch.float32, device=dev)
+    k_sc = torch.empty_like(q_sc)
+    vt = torch.empty((B, H, D, Sp), dtype=torch.uint8, device=dev)
+    v_sc = torch.empty((B, H, D), dtype=torch.float32, device=dev)
+    k_mean = torch.empty((B, H, D), dtype=torch.float32, device=dev)
+    with torch.cuda.device(dev):
+        _check(lib.sage_quantize_qkv_smooth_k(_ptr(q), _ptr(k), _ptr(v), B, S, H, D, _ptr(q_i8), _ptr(q_sc),
+                                              _ptr(k_i8), _ptr(k_sc), _ptr(vt), _ptr(v_sc), _ptr(k_mean),
+                                              _stream(dev)))
+    return q_i8, q_sc, k_i8, k_sc, vt, v_sc, k_mean
 
 
 def _quant_shape(q_i8, S):

@@ -1,0 +1,103 @@
+"""GPU parity of K smoothing (sage_quantize_qkv_smooth_k,
+sage_attn_fwd_smooth_k) against the oracle's reading R15.
+
+Source: InvokeAI PR #9657, "Summary" / "How it works" (SageAttention's
+smooth_k: per-channel K mean subtraction before quantisation).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from quantized_attention_diffusion_gb300.workloads import WORKLOADS, bf16_bits, make_workload, sample_rows
+from tests.gpu_common import assert_close_to_oracle, default_scale, ensure_library, f32, gen
+from tests.test_gpu_parity import SHAPES
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    return ensure_library()
+
+
+def _eq(name, g, r):
+    g = g.cpu().numpy() if isinstance(g, torch.Tensor) else g
+    assert g.shape == r.shape, name
+    eq = g.view(np.uint32) == r.view(np.uint32) if g.dtype == np.float32 else g == r
+    assert eq.all(), f"{name}: {int((~eq).sum())} mismatches, first at {np.argwhere(~eq)[0].tolist()}"
+
+
+def _check_quant(qkv, bits):
+    import quantized_attention_diffusion_gb300 as qad
+    q, k, v = [t.cuda() for t in qkv]
+    got = qad.quantize_qkv_smooth_k(q, k, v)
+    torch.cuda.synchronize()
+    qc, qs = oracle.quantize_qk(bits[0])
+    kc, ks, km = oracle.quantize_k_smooth(bits[1])
+    vt, vs = oracle.quantize_v(bits[2])
+    for name, g, r in zip(["q_i8", "q_scale", "k_i8", "k_scale", "vt", "v_scale", "k_mean"], got,
+                          [qc, qs, kc, ks, vt, vs, km]):
+        _eq(name, g, r)
+
+
+@pytest.mark.parametrize("B,S,H,recipe,seed", SHAPES)
+def test_smooth_k_quantisation_bit_exact(B, S, H, recipe, seed):
+    qkv, bits = gen(B, S, H, recipe, seed)
+    _check_quant(qkv, bits)
+
+
+def test_smooth_k_quantisation_full_size_4096x24_bit_exact():
+    qkv, bits = gen(1, 4096, 24, "k_channel_offset", 1)
+    _check_quant(qkv, bits)
+
+
+@pytest.mark.parametrize("B,S,H,recipe,seed", SHAPES)
+def test_smooth_k_attention_matches_oracle(B, S, H, recipe, seed):
+    import quantized_attention_diffusion_gb300 as qad
+    qkv, bits = gen(B, S, H, recipe, seed)
+    scale = default_scale()
+    out = qad.attn_fwd(*[t.cuda() for t in qkv], scale, smooth_k=True)
+    torch.cuda.synchronize()
+    ref, ties = oracle.attention(*bits, scale, return_ties=True, smooth_k=True)
+    assert_close_to_oracle(out.float().cpu().numpy(), f32(ref), ties, f"smooth B{B} S{S} H{H}")
+
+
+def test_exact_channel_offset_is_removed_on_gpu():
+    """Zero-mean integer keys plus an exact per-channel offset: smoothed
+    attention equals plain attention on the offset-free keys bit for bit."""
+    import quantized_attention_diffusion_gb300 as qad
+    B, S, H = 1, 256, 2
+    rng = np.random.default_rng(60)
+    half = rng.integers(-8, 9, size=(B, S // 2, H, 128)).astype(np.float32)
+    kz = np.concatenate([half, -half], axis=1)
+    c = rng.integers(-40, 41, size=(1, 1, H, 128)).astype(np.float32)
+    k0 = torch.from_numpy(kz).to(torch.bfloat16).cuda()
+    k1 = torch.from_numpy(kz + c).to(torch.bfloat16).cuda()
+    (q, _, v), _ = gen(B, S, H, "normal", 61)
+    q, v = q.cuda(), v.cuda()
+    plain = qad.attn_fwd(q, k0, v)
+    smooth = qad.attn_fwd(q, k1, v, smooth_k=True)
+    torch.cuda.synchronize()
+    assert torch.equal(plain.view(torch.int16), smooth.view(torch.int16))
+
+
+def test_smooth_k_full_size_sampled_rows():
+    """B=1 S=4096 H=24 with per-channel K offsets (where smoothing acts),
+    4 heads x 512 sampled rows against the oracle."""
+    import quantized_attention_diffusion_gb300 as qad
+    w = WORKLOADS["b1_s4096_h24_koffset"]
+    q, k, v = make_workload(w)
+    out = qad.attn_fwd(q.cuda(), k.cuda(), v.cuda(), w.softmax_scale, smooth_k=True)
+    torch.cuda.synchronize()
+    rows = sample_rows(w.B, w.S, w.H, heads=4, rows_per_head=512, seed=w.seed)
+    bits = [bf16_bits(t) for t in (q, k, v)]
+    quant = oracle.quantize(*bits, smooth_k=True)
+    ref, ties = oracle.attend_rows(quant, w.S, w.softmax_scale, rows, return_ties=True)
+    got = out.float().cpu().numpy()[rows[:, 0], rows[:, 2], rows[:, 1]]
+    err, _ = assert_close_to_oracle(got, f32(ref), ties, w.name)
+    print(f"{w.name} smooth_k: max-abs vs oracle {err:.4g}")
