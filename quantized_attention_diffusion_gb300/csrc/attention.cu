@@ -164,24 +164,6 @@ __device__ __forceinline__ void store_p_row(uint8_t* tile, int r, const uint32_t
         make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
 }
 
-// INT8 code of x for block scale sc, bit-identical to clamp(rint(x / sc),
-// -127, 127) with x / sc rounded to nearest even in fp32.  While 1/sc is a
-// normal float (sc in [2^-125, 2^125]), y = x * fl(1/sc) is within
-// |x/sc| * 2^-23 <= 1.6e-5 of x/sc (|x/sc| <= 127) and fl(x/sc) within
-// 7.6e-6, so both round to the same integer unless y lies within 2^-15 of a
-// half-integer; only then, or for extreme scales, is the division done.
-__device__ __forceinline__ int q_code(float x, float sc, float rcp) {
-  if (sc == 0.0f) return 0;
-  float y;
-  if (sc >= 0x1p-125f && sc <= 0x1p125f) {
-    y = x * rcp;
-    if (fabsf(y - floorf(y) - 0.5f) < 0x1p-15f) y = __fdiv_rn(x, sc);
-  } else {
-    y = __fdiv_rn(x, sc);
-  }
-  return static_cast<int>(fminf(fmaxf(rintf(y), -127.0f), 127.0f));
-}
-
 // One lane per row: quantise row r (0..127) of a bf16 Q tile in shared
 // memory (two 64-column halves, 128-byte swizzled rows) in place to
 // integer-valued fp16 codes.  The 32 lanes of the warp are one 32-row block:

@@ -28,11 +28,30 @@ namespace {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-__device__ __forceinline__ int qk_code(float v, float sc) {
-  if (sc == 0.0f) return 0;
-  float r = rintf(__fdiv_rn(v, sc));
-  r = fminf(fmaxf(r, -127.0f), 127.0f);
-  return static_cast<int>(r);
+// Rounding and code stores without the XU pipe (int/half conversions and
+// frnd there cap this HBM-bound kernel): y + 1.5*2^23 - 1.5*2^23 is y rounded
+// to the nearest integer, ties to even, exactly for |y| < 2^22, and the low
+// bits of y + 1.5*2^23 are that integer.
+constexpr float kRoundMagic = 12582912.0f;   // 1.5 * 2^23
+
+// Integer code of x for block scale sc, as a float: bit-identical to
+// clamp(rint(x / sc), -127, 127) with x / sc rounded to nearest even in fp32.
+// While 1/sc is a normal float (sc in [2^-125, 2^125]), y = x * fl(1/sc) is
+// within |x/sc| * 2^-23 <= 1.6e-5 of x/sc (|x/sc| <= 127) and fl(x/sc)
+// within 7.6e-6, so both round to the same integer unless y lies within
+// 2^-15 of a half-integer; only then, or for extreme scales, divide.
+__device__ __noinline__ float code_by_division(float x, float sc) {
+  const float y = __fdiv_rn(x, sc);
+  return fminf(fmaxf((y + kRoundMagic) - kRoundMagic, -127.0f), 127.0f);
+}
+
+__device__ __forceinline__ float code_f(float x, float sc, float rcp) {
+  if (sc == 0.0f) return 0.0f;
+  if (!(sc >= 0x1p-125f && sc <= 0x1p125f)) return code_by_division(x, sc);
+  const float y = x * rcp;
+  const float r = (y + kRoundMagic) - kRoundMagic;
+  if (fabsf(y - r) > 0.5f - 0x1p-15f) return code_by_division(x, sc);
+  return fminf(fmaxf(r, -127.0f), 127.0f);
 }
 
 template <typename CodeT>
@@ -40,25 +59,26 @@ struct CodeStore;
 
 template <>
 struct CodeStore<int8_t> {
-  // 8 codes -> 8 bytes
-  __device__ static void store(int8_t* dst, const int (&c)[8]) {
-    uint32_t lo = (c[0] & 0xFF) | ((c[1] & 0xFF) << 8) | ((c[2] & 0xFF) << 16) |
-                  (static_cast<uint32_t>(c[3] & 0xFF) << 24);
-    uint32_t hi = (c[4] & 0xFF) | ((c[5] & 0xFF) << 8) | ((c[6] & 0xFF) << 16) |
-                  (static_cast<uint32_t>(c[7] & 0xFF) << 24);
+  // 8 integer-valued floats -> 8 bytes (two's complement)
+  __device__ static void store(int8_t* dst, const float (&c)[8]) {
+    uint32_t b[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) b[i] = (__float_as_uint(c[i] + kRoundMagic) - 0x4B400000u) & 0xFFu;
+    const uint32_t lo = b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24);
+    const uint32_t hi = b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24);
     *reinterpret_cast<uint2*>(dst) = make_uint2(lo, hi);
   }
 };
 
 template <>
 struct CodeStore<__half> {
-  // 8 codes -> 8 integer-valued halves (exact for |c| <= 127)
-  __device__ static void store(__half* dst, const int (&c)[8]) {
+  // 8 integer-valued floats -> 8 halves (exact for |c| <= 127)
+  __device__ static void store(__half* dst, const float (&c)[8]) {
     uint32_t w[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      __half2 h2 = __halves2half2(__int2half_rn(c[2 * i]), __int2half_rn(c[2 * i + 1]));
-      w[i] = *reinterpret_cast<uint32_t*>(&h2);
+      const __half2 h2 = __floats2half2_rn(c[2 * i], c[2 * i + 1]);
+      w[i] = *reinterpret_cast<const uint32_t*>(&h2);
     }
     *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
   }
@@ -129,18 +149,19 @@ __global__ void __launch_bounds__(256) qk_quantize_kernel(QKQuantArgs<CodeT> a) 
                fmaxf(warp_max[sub * 4 + 2], warp_max[sub * 4 + 3]));
   if (!active) return;
   const float sc = __fdiv_rn(amax, 127.0f);
+  const float rcp = __frcp_rn(sc);
   if (w4 == 0 && lane == 0 && blk < nb) scale[static_cast<size_t>(bh) * nb + blk] = sc;
 
   CodeT* dst = codes + (static_cast<size_t>(bh) * S_pad + tok0) * kHeadDim + c8;
 #pragma unroll
   for (int it = 0; it < 4; ++it) {
     const uint32_t w[4] = {raw[it].x, raw[it].y, raw[it].z, raw[it].w};
-    int c[8];
+    float c[8];
     const bool valid = tok0 + 2 * it < S;   // rows past the end stay 0 (no -mean)
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      c[2 * i] = qk_code(smooth && valid ? bf16_lo(w[i]) - mu[2 * i] : bf16_lo(w[i]), sc);
-      c[2 * i + 1] = qk_code(smooth && valid ? bf16_hi(w[i]) - mu[2 * i + 1] : bf16_hi(w[i]), sc);
+      c[2 * i] = code_f(smooth && valid ? bf16_lo(w[i]) - mu[2 * i] : bf16_lo(w[i]), sc, rcp);
+      c[2 * i + 1] = code_f(smooth && valid ? bf16_hi(w[i]) - mu[2 * i + 1] : bf16_hi(w[i]), sc, rcp);
     }
     CodeStore<CodeT>::store(dst + static_cast<size_t>(2 * it) * kHeadDim, c);
   }

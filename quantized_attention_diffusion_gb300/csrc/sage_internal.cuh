@@ -82,4 +82,48 @@ void set_last_error(const char* fmt, ...);
 cudaError_t read_and_clear_device_error(int* code, cudaStream_t stream);
 cudaError_t launch_wait_timeout_probe(uint64_t timeout_ns, cudaStream_t stream);
 
+// ------------------------------------------------------ device helpers --
+// Shared by the quantisation and attention kernels.
+
+// INT8 code of x for block scale sc, bit-identical to clamp(rint(x / sc),
+// -127, 127) with x / sc rounded to nearest even in fp32.  While 1/sc is a
+// normal float (sc in [2^-125, 2^125]), y = x * fl(1/sc) is within
+// |x/sc| * 2^-23 <= 1.6e-5 of x/sc (|x/sc| <= 127) and fl(x/sc) within
+// 7.6e-6, so both round to the same integer unless y lies within 2^-15 of a
+// half-integer; only then, or for extreme scales, is the division done.
+__device__ __forceinline__ int q_code(float x, float sc, float rcp) {
+  if (sc == 0.0f) return 0;
+  float y;
+  if (sc >= 0x1p-125f && sc <= 0x1p125f) {
+    y = x * rcp;
+    if (fabsf(y - floorf(y) - 0.5f) < 0x1p-15f) y = __fdiv_rn(x, sc);
+  } else {
+    y = __fdiv_rn(x, sc);
+  }
+  return static_cast<int>(fminf(fmaxf(rintf(y), -127.0f), 127.0f));
+}
+
+// Two fp32 values -> two E4M3 codes (round to nearest even, saturating):
+// `lo` lands in the low byte.
+__device__ __forceinline__ uint16_t e4m3x2_rn(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// E4M3 code of x / s (s > 0), bit-identical to encoding the fp32-RNE
+// quotient.  While 1/s is a normal float, y = x * fl(1/s) is within
+// 3 * 2^-24 (relative) of the exact quotient and fl(x / s) within 2^-24, so
+// when y * (1 - 2^-21) and y * (1 + 2^-21) encode alike, every value between
+// them, the quotient included, encodes alike (rounding is monotonic);
+// otherwise, or for extreme scales, divide.
+__device__ __forceinline__ uint8_t e4m3_of_quotient(float x, float s, float rcp) {
+  if (!(s >= 0x1p-125f && s <= 0x1p125f))
+    return static_cast<uint8_t>(e4m3x2_rn(__fdiv_rn(x, s), 0.0f) & 0xFFu);
+  const float y = x * rcp;
+  const uint16_t pair = e4m3x2_rn(y * (1.0f - 0x1p-21f), y * (1.0f + 0x1p-21f));
+  if ((pair & 0xFFu) == (pair >> 8)) return static_cast<uint8_t>(pair & 0xFFu);
+  return static_cast<uint8_t>(e4m3x2_rn(__fdiv_rn(x, s), 0.0f) & 0xFFu);
+}
+
 }  // namespace sage
