@@ -103,27 +103,4 @@ __device__ __forceinline__ int q_code(float x, float sc, float rcp) {
   return static_cast<int>(fminf(fmaxf(rintf(y), -127.0f), 127.0f));
 }
 
-// Two fp32 values -> two E4M3 codes (round to nearest even, saturating):
-// `lo` lands in the low byte.
-__device__ __forceinline__ uint16_t e4m3x2_rn(float lo, float hi) {
-  uint16_t r;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-  return r;
-}
-
-// E4M3 code of x / s (s > 0), bit-identical to encoding the fp32-RNE
-// quotient.  While 1/s is a normal float, y = x * fl(1/s) is within
-// 3 * 2^-24 (relative) of the exact quotient and fl(x / s) within 2^-24, so
-// when y * (1 - 2^-21) and y * (1 + 2^-21) encode alike, every value between
-// them, the quotient included, encodes alike (rounding is monotonic);
-// otherwise, or for extreme scales, divide.
-__device__ __forceinline__ uint8_t e4m3_of_quotient(float x, float s, float rcp) {
-  if (!(s >= 0x1p-125f && s <= 0x1p125f))
-    return static_cast<uint8_t>(e4m3x2_rn(__fdiv_rn(x, s), 0.0f) & 0xFFu);
-  const float y = x * rcp;
-  const uint16_t pair = e4m3x2_rn(y * (1.0f - 0x1p-21f), y * (1.0f + 0x1p-21f));
-  if ((pair & 0xFFu) == (pair >> 8)) return static_cast<uint8_t>(pair & 0xFFu);
-  return static_cast<uint8_t>(e4m3x2_rn(__fdiv_rn(x, s), 0.0f) & 0xFFu);
-}
-
 }  // namespace sage
