@@ -457,11 +457,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       float mt = -INFINITY;
 #pragma unroll
-      for (int i = 0; i < 3; ++i) {
-        float mx = a[32 * i];
+      for (int i = 0; i < 3; ++i) {       // four independent chains per K block
+        const float* ab = a + 32 * i;
+        float m0 = ab[0], m1 = ab[1], m2 = ab[2], m3 = ab[3];
 #pragma unroll
-        for (int c = 1; c < 31; c += 2) mx = fmax3(mx, a[32 * i + c], a[32 * i + c + 1]);
-        mx = fmaxf(mx, a[32 * i + 31]);
+        for (int c = 4; c < 28; c += 8) {
+          m0 = fmax3(m0, ab[c], ab[c + 1]);
+          m1 = fmax3(m1, ab[c + 2], ab[c + 3]);
+          m2 = fmax3(m2, ab[c + 4], ab[c + 5]);
+          m3 = fmax3(m3, ab[c + 6], ab[c + 7]);
+        }
+        m0 = fmax3(m0, ab[28], ab[29]);
+        m1 = fmax3(m1, ab[30], ab[31]);
+        const float mx = fmax3(m0, m1, fmaxf(m2, m3));
         mt = fmaxf(mt, mx * cb[i]);       // a block past the end gives -inf or NaN: ignored
       }
       const float m_new = fmaxf(m_run, mt);
