@@ -153,6 +153,16 @@ __device__ __forceinline__ void softmax_p(const float (&a)[kKV], const float (&c
   }
 }
 
+// 32 TMEM columns (as loaded) times alpha, on the packed FP32 pipe.
+__device__ __forceinline__ void scale_cols(uint32_t (&o)[32], float alpha) {
+#pragma unroll
+  for (int i = 0; i < 32; i += 2) {
+    const float2 r = fmul2(__uint_as_float(o[i]), __uint_as_float(o[i + 1]), alpha);
+    o[i] = __float_as_uint(r.x);
+    o[i + 1] = __float_as_uint(r.y);
+  }
+}
+
 // Row r of a P~ tile in the 128-byte-swizzled K-major layout: 16-byte chunk
 // c of row r sits at (r/8)*1024 + (r%8)*128 + (c ^ (r%8))*16.  Chunks 0-5
 // hold the 96 codes.
@@ -489,32 +499,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after();
+      store_p_row(sP + t * kPTileBytes, row, pk);
       // Rescale O and L when the running max moved.
       const bool need = (j > 0) && (m_new != m_run);
       if (__any_sync(0xFFFFFFFFu, need)) {
+        // Two rounds of loads (64 columns, then 64 + L) so that only two
+        // TMEM load latencies are exposed; the score registers are dead here.
         const float alpha = ex2_approx(m_run - m_new);
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t o[32];
-          tmem_ld32(tO + c * 32, o);
-          tmem_ld_wait();
-#pragma unroll
-          for (int i = 0; i < 32; i += 2) {
-            const float2 r = fmul2(__uint_as_float(o[i]), __uint_as_float(o[i + 1]), alpha);
-            o[i] = __float_as_uint(r.x);
-            o[i + 1] = __float_as_uint(r.y);
-          }
-          tmem_st32(tO + c * 32, o);
-        }
-        uint32_t l4[4];
-        tmem_ld4(tO + 128, l4);
+        uint32_t o0[32], o1[32], o2[32], o3[32], l4[4];
+        tmem_ld32(tO, o0);
+        tmem_ld32(tO + 32, o1);
         tmem_ld_wait();
+        tmem_ld32(tO + 64, o2);
+        tmem_ld32(tO + 96, o3);
+        tmem_ld4(tO + 128, l4);
+        scale_cols(o0, alpha);
+        tmem_st32(tO, o0);
+        scale_cols(o1, alpha);
+        tmem_st32(tO + 32, o1);
+        tmem_ld_wait();
+        scale_cols(o2, alpha);
+        tmem_st32(tO + 64, o2);
+        scale_cols(o3, alpha);
+        tmem_st32(tO + 96, o3);
         l4[0] = __float_as_uint(__uint_as_float(l4[0]) * alpha);
         tmem_st4(tO + 128, l4);
         tmem_st_wait();
       }
       m_run = m_new;
-      store_p_row(sP + t * kPTileBytes, row, pk);
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // P~ visible to the MMA
       tc_fence_before();
       mbar_arrive(&bars.p_full[t]);
