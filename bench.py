@@ -101,6 +101,12 @@ class Group:
             self.dist.destroy_process_group()
 
 
+def job_tops(world: int, ops_per_call: float, calls_per_rank: int, ms_max: float) -> float:
+    """Whole-job throughput of weak-scaled replicas: every rank runs the
+    same number of calls; the slowest rank's time bounds the job."""
+    return world * ops_per_call * calls_per_rank / (ms_max * 1e-3) / 1e12
+
+
 # --------------------------------------------------------------- clocks --
 
 class ClockSampler:
@@ -290,7 +296,7 @@ def run_ours(args, group, local):
     attn_ms = statistics.mean(b.elapsed_time(a) for b, a in zip(before, after))
     ms_max = group.max(ms)
     attn_ms_max = group.max(attn_ms)
-    value = group.world * w.ops * K / (ms_max * 1e-3) / 1e12
+    value = job_tops(group.world, w.ops, K, ms_max)
 
     # End to end through the public API with host buffers: every step copies
     # its Q/K/V from pinned host memory to the device, runs the step and
@@ -349,7 +355,7 @@ def run_ours(args, group, local):
         torch.cuda.synchronize()
         group.barrier()
         e2e_ms = group.max(s2.elapsed_time(e2))
-        e2e_value = group.world * w.ops * K2 / (e2e_ms * 1e-3) / 1e12
+        e2e_value = job_tops(group.world, w.ops, K2, e2e_ms)
     in_bytes = (q.numel() + k.numel() + v.numel()) * q.element_size()
     out_bytes = out.numel() * out.element_size() + (lse.numel() * 4 if args.lse else 0)
 
