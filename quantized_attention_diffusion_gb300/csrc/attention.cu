@@ -22,9 +22,10 @@
 //
 // One CTA owns two 128-row Q tiles of one (batch, head) and streams every KV
 // tile of that head.  384 threads:
-//   warp 0       TMA producer (Q once; K and V^T through 3-stage rings)
+//   warp 0       TMA producer of Q (once) and K (3-stage ring)
 //   warp 1       TMEM allocator; issues the QK^T MMAs (one thread)
 //   warp 2       issues the PV MMAs (one thread)
+//   warp 3       TMA producer of V^T (4-stage ring, 32-byte swizzle)
 //   warps 2-3    first write the ones rows of the V stages
 //   warps 4-7    softmax + epilogue of Q tile 0, one thread per query row
 //   warps 8-11   the same for Q tile 1
@@ -68,14 +69,20 @@ constexpr uint32_t kQHalf = 128 * 64 * 2;                // 128 rows x 64 fp16
 constexpr uint32_t kQTileBytes = 2 * kQHalf;
 constexpr uint32_t kKHalf = kKV * 64 * 2;                // 96 rows x 64 fp16
 constexpr uint32_t kKTileBytes = 2 * kKHalf;
-constexpr uint32_t kVTileBytes = 128 * 128;              // V^T: 128 channels x 128 keys (96 used)
-constexpr uint32_t kOnesBytes = 16 * 128;                // 16 rows of E4M3 1.0
-constexpr uint32_t kVStageBytes = kVTileBytes + kOnesBytes;
+constexpr int kVStages = 4;                               // V^T ring depth (K ring: kStages)
+// A V^T stage holds one KV tile as three 32-key sub-tiles (one per K=32 step
+// of the PV MMA), each 144 rows x 32 bytes with 32-byte swizzle: V^T's 128
+// channel rows, then 16 rows of E4M3 ones.  Only the 96 keys of the tile
+// are loaded, which is what makes room for four stages.
+constexpr uint32_t kVSubBytes = 144 * 32;
+constexpr uint32_t kVOnesOffset = 128 * 32;              // ones rows within a sub-tile
+constexpr uint32_t kVStageBytes = 3 * kVSubBytes;
+constexpr uint32_t kVLoadBytes = 3 * 128 * 32;           // bytes TMA writes per stage
 constexpr uint32_t kPTileBytes = 128 * 128;              // P~: 128 rows x 128 bytes (96 used)
 constexpr uint32_t kSmemQ = 0;
 constexpr uint32_t kSmemK = kSmemQ + 2 * kQTileBytes;
 constexpr uint32_t kSmemV = kSmemK + kStages * kKTileBytes;
-constexpr uint32_t kSmemP = kSmemV + kStages * kVStageBytes;
+constexpr uint32_t kSmemP = kSmemV + kVStages * kVStageBytes;
 constexpr uint32_t kSmemTiles = kSmemP + 2 * kPTileBytes;
 constexpr uint32_t kSmemDynamic = kSmemTiles + 1024;     // slack for 1024-byte alignment
 // TMEM columns of tile t's scores (96) and accumulator (144; L at +128).
@@ -107,7 +114,7 @@ struct Params {
 struct Barriers {
   uint64_t q_full, q_ready;
   uint64_t k_full[kStages], k_empty[kStages];
-  uint64_t v_full[kStages], v_empty[kStages];
+  uint64_t v_full[kVStages], v_empty[kVStages];
   uint64_t s_full[2], s_free[2], p_full[2], pv_done[2], o_full[2];
   uint64_t drain_qk, drain_pv;
 };
@@ -251,6 +258,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&bars.k_full[s], 1);
       mbar_init(&bars.k_empty[s], 1);
+    }
+    for (int s = 0; s < kVStages; ++s) {
       mbar_init(&bars.v_full[s], 1);
       mbar_init(&bars.v_empty[s], 1);
     }
@@ -273,9 +282,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 2 || warp == 3) {
     // Rows 128..143 of every V stage: E4M3 ones (any swizzle of equal bytes is
     // the same), the extra N rows that make PV also sum P.
-    for (uint32_t i = threadIdx.x - 64; i < kStages * kOnesBytes / 4; i += 64) {
-      const uint32_t s = i / (kOnesBytes / 4), w = i % (kOnesBytes / 4);
-      reinterpret_cast<uint32_t*>(sV + s * kVStageBytes + kVTileBytes)[w] = kE4M3One;
+    constexpr uint32_t kOnesWords = 16 * 32 / 4;   // per sub-tile
+    for (uint32_t i = threadIdx.x - 64; i < kVStages * 3 * kOnesWords; i += 64) {
+      const uint32_t sub = i / kOnesWords, w = i % kOnesWords;
+      reinterpret_cast<uint32_t*>(sV + sub * kVSubBytes + kVOnesOffset)[w] = kE4M3One;
     }
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
@@ -302,7 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_3d(sQ + t * kQTileBytes + kQHalf, &tmQ, &bars.q_full, 64, q_row0 + t * kTile, bh);
         }
       }
-      int k_issued = 0, v_issued = 0;
+      int k_issued = 0;
       for (int j = 0; j < p.n_kv; ++j) {
         const int s = j % kStages, r = j / kStages;
         if (r > 0 && !wait_bar(&bars.k_empty[s], (r - 1) & 1, abort_v, p.timeout_ns)) break;
@@ -310,17 +320,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_3d(sK + s * kKTileBytes, &tmK, &bars.k_full[s], 0, j * kKV, bh);
         tma_load_3d(sK + s * kKTileBytes + kKHalf, &tmK, &bars.k_full[s], 64, j * kKV, bh);
         k_issued = j + 1;
-        if (r > 0 && !wait_bar(&bars.v_empty[s], (r - 1) & 1, abort_v, p.timeout_ns)) break;
-        mbar_arrive_expect_tx(&bars.v_full[s], kVTileBytes);
-        tma_load_3d(sV + s * kVStageBytes, &tmV, &bars.v_full[s], j * kKV, 0, bh);
-        v_issued = j + 1;
       }
       // Let every issued copy land before the CTA can exit.
       drain_bar(&bars.q_full, 0, p.timeout_ns);
       for (int j = k_issued - 1; j >= 0 && j >= k_issued - kStages; --j)
         drain_bar(&bars.k_full[j % kStages], (j / kStages) & 1, p.timeout_ns);
-      for (int j = v_issued - 1; j >= 0 && j >= v_issued - kStages; --j)
-        drain_bar(&bars.v_full[j % kStages], (j / kStages) & 1, p.timeout_ns);
+    }
+  } else if (warp == 3) {
+    // ---------------------------------------------------- V^T producer --
+    // Its own thread, so that a V stage still in use never holds up K.
+    if (lane == 0) {
+      int v_issued = 0;
+      for (int j = 0; j < p.n_kv; ++j) {
+        const int s = j % kVStages, r = j / kVStages;
+        if (r > 0 && !wait_bar(&bars.v_empty[s], (r - 1) & 1, abort_v, p.timeout_ns)) break;
+        mbar_arrive_expect_tx(&bars.v_full[s], kVLoadBytes);
+#pragma unroll
+        for (int k = 0; k < 3; ++k)
+          tma_load_3d(sV + s * kVStageBytes + k * kVSubBytes, &tmV, &bars.v_full[s], j * kKV + 32 * k, 0, bh);
+        v_issued = j + 1;
+      }
+      for (int j = v_issued - 1; j >= 0 && j >= v_issued - kVStages; --j)
+        drain_bar(&bars.v_full[j % kVStages], (j / kVStages) & 1, p.timeout_ns);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------ QK^T issuer --
@@ -362,8 +383,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t idesc = make_idesc_f32acc(128, 144, 0, 0);   // E4M3 x E4M3 -> F32
       const uint32_t p_lo = sw128_desc_lo(smem_addr(sP)), v_lo = sw128_desc_lo(smem_addr(sV));
       for (int j = 0; j < p.n_kv; ++j) {
-        const int s = j % kStages;
-        if (!wait_bar(&bars.v_full[s], (j / kStages) & 1, abort_v, p.timeout_ns)) break;
+        const int s = j % kVStages;
+        if (!wait_bar(&bars.v_full[s], (j / kVStages) & 1, abort_v, p.timeout_ns)) break;
         const uint32_t b0 = v_lo + s * (kVStageBytes >> 4);
         bool ok = true;
 #pragma unroll
@@ -375,7 +396,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           const uint32_t a0 = p_lo + t * (kPTileBytes >> 4);
 #pragma unroll
-          for (int k = 0; k < 3; ++k) mma_f8_ss(tmem + col_o(t), a0 + 2 * k, b0 + 2 * k, idesc, (j > 0 || k > 0));
+          for (int k = 0; k < 3; ++k)
+            mma_f8_ss(tmem + col_o(t), a0 + 2 * k, b0 + k * (kVSubBytes >> 4), idesc, (j > 0 || k > 0), kSw32DescHi);
           mma_commit(&bars.pv_done[t]);
         }
         if (!ok) break;
@@ -589,7 +611,8 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 // 3-D map over [BH][rows][inner] with a box of box_inner x box_rows x 1 and
 // 128-byte swizzle.
 bool encode_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, uint32_t esize,
-                uint64_t inner, uint64_t rows, uint64_t bh, uint32_t box_inner, uint32_t box_rows) {
+                uint64_t inner, uint64_t rows, uint64_t bh, uint32_t box_inner, uint32_t box_rows,
+                CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   auto enc = tensor_map_encoder();
   if (!enc) return false;
   std::memset(m, 0, sizeof(*m));
@@ -598,7 +621,7 @@ bool encode_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, uint32
   cuuint32_t box[3] = {box_inner, box_rows, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   return enc(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -645,7 +668,8 @@ cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream) {
                                         64, 128);
   if (!qmap_ok ||
       !encode_map(&tmK, a.k_codes, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, kHeadDim, a.Skv_pad, BH, 64, kKV) ||
-      !encode_map(&tmV, a.vt, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.Skv_pad, kHeadDim, BH, 128, 128))
+      !encode_map(&tmV, a.vt, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.Skv_pad, kHeadDim, BH, 32, 128,
+                  CU_TENSOR_MAP_SWIZZLE_32B))
     return cudaErrorInvalidValue;
   Params p;
   p.fuse_q = a.q_bf16 != nullptr;

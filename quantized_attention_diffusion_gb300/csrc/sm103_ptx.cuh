@@ -179,14 +179,19 @@ __device__ __forceinline__ void mma_f16_ss(uint32_t d_tmem, uint32_t a_lo, uint3
       : "memory");
 }
 
-// D[tmem] (+)= A[smem] * B[smem]^T, kind::f8f6f4 (one K=32 step).
+// Upper word of a descriptor for a K-major operand with 32-byte rows and
+// 32-byte swizzling (8-row groups 256 bytes apart, swizzle mode 6).
+constexpr uint32_t kSw32DescHi = (256u >> 4) | (1u << 14) | (6u << 29);
+
+// D[tmem] (+)= A[smem] * B[smem]^T, kind::f8f6f4 (one K=32 step); A with
+// 128-byte swizzle, B with the layout whose upper descriptor word is b_hi.
 __device__ __forceinline__ void mma_f8_ss(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t idesc,
-                                          uint32_t accumulate) {
+                                          uint32_t accumulate, uint32_t b_hi = kSw128DescHi) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "mov.b64 da, {%1, %5};\n\tmov.b64 db, {%2, %5};\n\t"
+      "mov.b64 da, {%1, %5};\n\tmov.b64 db, {%2, %6};\n\t"
       "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], da, db, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_lo), "r"(b_lo), "r"(idesc), "r"(accumulate), "r"(kSw128DescHi)
+      "r"(a_lo), "r"(b_lo), "r"(idesc), "r"(accumulate), "r"(kSw128DescHi), "r"(b_hi)
       : "memory");
 }
 
