@@ -94,6 +94,10 @@ constexpr float kLn2 = 0.693147182464599609375f;          // fp32(ln 2)
 constexpr uint32_t kE4M3One = 0x38383838u;                // four E4M3 1.0
 
 static_assert(kSmemDynamic <= 227 * 1024 - 1024, "shared memory budget");
+static_assert(kSmemQ % 1024 == 0 && kSmemK % 1024 == 0 && kSmemP % 1024 == 0 && kKTileBytes % 1024 == 0 &&
+                  kQHalf % 1024 == 0 && kKHalf % 1024 == 0 && kPTileBytes % 1024 == 0,
+              "128-byte swizzle atoms are 1024-byte aligned");
+static_assert(kSmemV % 256 == 0 && kVSubBytes % 256 == 0, "32-byte swizzle atoms are 256-byte aligned");
 
 struct Params {
   int fuse_q;             // 1: Q arrives as bf16 and is quantised here (q_scale unused)
