@@ -45,13 +45,36 @@ __device__ __noinline__ float code_by_division(float x, float sc) {
   return fminf(fmaxf((y + kRoundMagic) - kRoundMagic, -127.0f), 127.0f);
 }
 
-__device__ __forceinline__ float code_f(float x, float sc, float rcp) {
-  if (sc == 0.0f) return 0.0f;
-  if (!(sc >= 0x1p-125f && sc <= 0x1p125f)) return code_by_division(x, sc);
-  const float y = x * rcp;
-  const float r = (y + kRoundMagic) - kRoundMagic;
-  if (fabsf(y - r) > 0.5f - 0x1p-15f) return code_by_division(x, sc);
-  return fminf(fmaxf(r, -127.0f), 127.0f);
+// Eight codes at once on the packed FP32 pipe, for a block scale sc in
+// [2^-125, 2^125] (rcp = fl(1/sc)).  No clamp: |x| <= amax = 127 sc (1 + 2^-24)
+// at most, so |y| < 127.5 and the rounded code is within [-127, 127].
+// Returns false when some y lies within 2^-15 of a half-integer (or is not
+// finite); the caller then divides, value by value.
+__device__ __forceinline__ bool codes8_fast(const float (&x)[8], float rcp, float (&c)[8]) {
+  constexpr float kTieLimit = 0.5f - 0x1p-15f;
+  const float2 m2 = make_float2(kRoundMagic, kRoundMagic), r2 = make_float2(rcp, rcp);
+  bool ok = true;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 y = fmul2v(make_float2(x[2 * i], x[2 * i + 1]), r2);
+    const float2 r = fsub2v(fadd2v(y, m2), m2);
+    const float2 d = fsub2v(y, r);
+    ok &= (fabsf(d.x) <= kTieLimit) & (fabsf(d.y) <= kTieLimit);
+    c[2 * i] = r.x;
+    c[2 * i + 1] = r.y;
+  }
+  return ok;
+}
+
+// Codes of eight values of one block with scale sc (rcp = fl(1/sc)).
+__device__ __forceinline__ void codes8(const float (&x)[8], float sc, float rcp, bool fast_sc, float (&c)[8]) {
+  if (sc == 0.0f) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) c[e] = 0.0f;
+  } else if (!(fast_sc && codes8_fast(x, rcp, c))) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) c[e] = code_by_division(x[e], sc);
+  }
 }
 
 template <typename CodeT>
@@ -150,19 +173,21 @@ __global__ void __launch_bounds__(256) qk_quantize_kernel(QKQuantArgs<CodeT> a) 
   if (!active) return;
   const float sc = __fdiv_rn(amax, 127.0f);
   const float rcp = __frcp_rn(sc);
+  const bool fast_sc = sc >= 0x1p-125f && sc <= 0x1p125f;
   if (w4 == 0 && lane == 0 && blk < nb) scale[static_cast<size_t>(bh) * nb + blk] = sc;
 
   CodeT* dst = codes + (static_cast<size_t>(bh) * S_pad + tok0) * kHeadDim + c8;
 #pragma unroll
   for (int it = 0; it < 4; ++it) {
     const uint32_t w[4] = {raw[it].x, raw[it].y, raw[it].z, raw[it].w};
-    float c[8];
+    float xs[8], c[8];
     const bool valid = tok0 + 2 * it < S;   // rows past the end stay 0 (no -mean)
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      c[2 * i] = code_f(smooth && valid ? bf16_lo(w[i]) - mu[2 * i] : bf16_lo(w[i]), sc, rcp);
-      c[2 * i + 1] = code_f(smooth && valid ? bf16_hi(w[i]) - mu[2 * i + 1] : bf16_hi(w[i]), sc, rcp);
+      xs[2 * i] = smooth && valid ? bf16_lo(w[i]) - mu[2 * i] : bf16_lo(w[i]);
+      xs[2 * i + 1] = smooth && valid ? bf16_hi(w[i]) - mu[2 * i + 1] : bf16_hi(w[i]);
     }
+    codes8(xs, sc, rcp, fast_sc, c);
     CodeStore<CodeT>::store(dst + static_cast<size_t>(2 * it) * kHeadDim, c);
   }
 }
