@@ -285,55 +285,83 @@ __global__ void k_mean_kernel(const unsigned long long* __restrict__ sums, int S
   }
 }
 
+// E4M3 codes of x0 / sv0 and x1 / sv1 (low byte first), bit-identical to
+// converting the correctly rounded quotients.  With rcp = fl(1/sv) for sv in
+// [2^-125, 2^125], y = x * rcp lies within 3 * 2^-24 relative of fl(x / sv),
+// so y (1 - 2^-20) and y (1 + 2^-20) bracket it; the conversion is monotonic,
+// so equal codes at both ends are the code of fl(x / sv).  Otherwise divide.
+__device__ __forceinline__ uint16_t e4m3_code2(float x0, float x1, float sv0, float sv1, float2 rcp, bool fast) {
+  if (fast) {
+    const float2 y = fmul2v(make_float2(x0, x1), rcp);
+    const float2 lo = fmul2v(y, make_float2(1.0f - 0x1p-20f, 1.0f - 0x1p-20f));
+    const float2 hi = fmul2v(y, make_float2(1.0f + 0x1p-20f, 1.0f + 0x1p-20f));
+    const uint16_t c_lo = cvt_e4m3x2(lo.x, lo.y), c_hi = cvt_e4m3x2(hi.x, hi.y);
+    if (c_lo == c_hi) return c_lo;
+  }
+  return cvt_e4m3x2(sv0 == 0.0f ? 0.0f : __fdiv_rn(x0, sv0), sv1 == 0.0f ? 0.0f : __fdiv_rn(x1, sv1));
+}
+
 // Encode one 128-token tile of one (batch, head) and write it transposed.
-// grid = (S_pad / 128, B*H), 256 threads.  Tokens >= S get code 0.
+// grid = (S_pad / 128, B*H), 256 threads.  Warp w owns channels 16w .. +15;
+// its lane l owns channels 16w + 4*(l%4) .. +3 of tokens 16*(l/4) .. +15.  A
+// load instruction of the warp reads eight whole 32-byte sectors (16
+// channels of 8 tokens); after encoding, a 4x4 byte transpose in registers
+// gives each lane 16 tokens of each of its 4 channels, so a store
+// instruction writes 4 channel rows x 128 contiguous bytes.  All loads are
+// issued before any encoding.  Tokens >= S get code 0.
 __global__ void __launch_bounds__(256) v_encode_kernel(const uint16_t* __restrict__ v, int S, int H,
                                                        int S_pad,
                                                        const uint32_t* __restrict__ amax_bits,
                                                        uint8_t* __restrict__ vt,
                                                        float* __restrict__ v_scale) {
-  constexpr int kPitch = 132;  // bytes per transposed row (word aligned)
-  __shared__ float sv[kHeadDim];
-  __shared__ __align__(16) uint8_t tile[kHeadDim * kPitch];
   const int bh = blockIdx.y, b = bh / H, h = bh % H;
-  const int tok0 = blockIdx.x * 128;
-  const int t = threadIdx.x;
-  if (t < kHeadDim) {
-    const float s = __fdiv_rn(__uint_as_float(amax_bits[static_cast<size_t>(bh) * kHeadDim + t]), 448.0f);
-    sv[t] = s;
-    if (blockIdx.x == 0) v_scale[static_cast<size_t>(bh) * kHeadDim + t] = s;
-  }
-  __syncthreads();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int c4 = warp * 16 + (lane & 3) * 4;
+  const int s0 = blockIdx.x * 128 + (lane >> 2) * 16;
   const size_t tok_stride = static_cast<size_t>(H) * kHeadDim;
-  const uint16_t* src = v + (static_cast<size_t>(b) * S * H + h) * kHeadDim;
-#pragma unroll 2
-  for (int k = 0; k < 8; ++k) {
-    const int chunk = k * 256 + t;
-    const int row = chunk >> 4, c8 = (chunk & 15) * 8;
-    const int s = tok0 + row;
-    uint4 q = make_uint4(0, 0, 0, 0);
-    if (s < S) q = __ldcs(reinterpret_cast<const uint4*>(src + static_cast<size_t>(s) * tok_stride + c8));
-    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+  const uint16_t* src = v + (static_cast<size_t>(b) * S * H + h) * kHeadDim + c4;
+  uint2 raw[16];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int d = c8 + 2 * i;
-      const float y0 = sv[d] == 0.0f ? 0.0f : __fdiv_rn(bf16_lo(w[i]), sv[d]);
-      const float y1 = sv[d + 1] == 0.0f ? 0.0f : __fdiv_rn(bf16_hi(w[i]), sv[d + 1]);
-      const uint16_t pair = cvt_e4m3x2(y0, y1);
-      tile[d * kPitch + row] = static_cast<uint8_t>(pair & 0xFF);
-      tile[(d + 1) * kPitch + row] = static_cast<uint8_t>(pair >> 8);
-    }
+  for (int i = 0; i < 16; ++i) {
+    const int s = s0 + i;
+    raw[i] = s < S ? __ldcs(reinterpret_cast<const uint2*>(src + static_cast<size_t>(s) * tok_stride))
+                   : make_uint2(0, 0);
   }
-  __syncthreads();
-  uint8_t* dst = vt + static_cast<size_t>(bh) * kHeadDim * S_pad + tok0;
+  float sv[4];
+  bool fast = true;
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const int chunk = k * 256 + t;
-    const int d = chunk >> 3, c16 = (chunk & 7) * 16;
-    const uint32_t* srow = reinterpret_cast<const uint32_t*>(tile + d * kPitch + c16);
-    *reinterpret_cast<uint4*>(dst + static_cast<size_t>(d) * S_pad + c16) =
-        make_uint4(srow[0], srow[1], srow[2], srow[3]);
+  for (int c = 0; c < 4; ++c) {
+    sv[c] = __fdiv_rn(__uint_as_float(amax_bits[static_cast<size_t>(bh) * kHeadDim + c4 + c]), 448.0f);
+    fast &= sv[c] >= 0x1p-125f && sv[c] <= 0x1p125f;
   }
+  const float2 rcp01 = make_float2(__frcp_rn(sv[0]), __frcp_rn(sv[1]));
+  const float2 rcp23 = make_float2(__frcp_rn(sv[2]), __frcp_rn(sv[3]));
+  if (blockIdx.x == 0 && (lane >> 2) == 0)
+    *reinterpret_cast<float4*>(v_scale + static_cast<size_t>(bh) * kHeadDim + c4) =
+        make_float4(sv[0], sv[1], sv[2], sv[3]);
+  uint32_t tok[16];   // tok[i]: the codes of token s0+i, channel c4+k in byte k
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const uint32_t lo = e4m3_code2(bf16_lo(raw[i].x), bf16_hi(raw[i].x), sv[0], sv[1], rcp01, fast);
+    const uint32_t hi = e4m3_code2(bf16_lo(raw[i].y), bf16_hi(raw[i].y), sv[2], sv[3], rcp23, fast);
+    tok[i] = lo | (hi << 16);
+  }
+  uint32_t row[4][4];   // row[c][g]: tokens 4g..4g+3 of channel c4+c
+#pragma unroll
+  for (int g = 0; g < 4; ++g) {
+    const uint32_t* w = tok + 4 * g;
+    const uint32_t a01 = __byte_perm(w[0], w[1], 0x5140), b01 = __byte_perm(w[0], w[1], 0x7362);
+    const uint32_t a23 = __byte_perm(w[2], w[3], 0x5140), b23 = __byte_perm(w[2], w[3], 0x7362);
+    row[0][g] = __byte_perm(a01, a23, 0x5410);
+    row[1][g] = __byte_perm(a01, a23, 0x7632);
+    row[2][g] = __byte_perm(b01, b23, 0x5410);
+    row[3][g] = __byte_perm(b01, b23, 0x7632);
+  }
+  uint8_t* dst = vt + (static_cast<size_t>(bh) * kHeadDim + c4) * S_pad + s0;
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+    *reinterpret_cast<uint4*>(dst + static_cast<size_t>(c) * S_pad) =
+        make_uint4(row[c][0], row[c][1], row[c][2], row[c][3]);
 }
 
 // int8 codes -> integer-valued fp16 codes, 16 per thread.
