@@ -107,78 +107,75 @@ struct CodeStore<__half> {
   }
 };
 
-// Four warps per (tensor, batch*head, 32-token block); a CTA of 256 threads
-// takes two blocks.  Warp w (0..3 within its block) owns tokens [8w, 8w+8):
-// lanes 0-15 the even token of a pair, lanes 16-31 the odd one, lane%16 owns
-// channels 8*(lane%16) .. +7.  The block max is a warp shuffle then a
-// shared-memory max over the four warps.  grid.y selects Q (0) or K (1).
+// One warp per (tensor, batch*head, 32-token block), eight blocks per CTA of
+// 256 threads.  Lanes 0-15 own the even tokens of the block, lanes 16-31 the
+// odd ones, lane%16 owns channels 8*(lane%16) .. +7: a load or store
+// instruction of the warp covers two whole 256-byte token rows.  A lane loads
+// all its 16 tokens before anything else (256 bytes in flight), and the block
+// max is a warp shuffle: no shared memory, no block-wide barrier.  grid.y
+// selects Q (0) or K (1).
 template <typename CodeT, bool kSmooth>
-__global__ void __launch_bounds__(256) qk_quantize_kernel(QKQuantArgs<CodeT> a) {
-  __shared__ float warp_max[8];
+__global__ void __launch_bounds__(256, 2) qk_quantize_kernel(QKQuantArgs<CodeT> a) {
   const int tensor = blockIdx.y + a.first;
   const uint16_t* __restrict__ x = tensor == 0 ? a.q : a.k;
   CodeT* __restrict__ codes = tensor == 0 ? a.q_codes : a.k_codes;
   float* __restrict__ scale = tensor == 0 ? a.q_scale : a.k_scale;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int sub = warp >> 2, w4 = warp & 3;
   const int S = a.S[tensor], S_pad = a.S_pad[tensor], nb = a.nb[tensor];
   const int nbp = S_pad / 32;
-  const long long gblk = static_cast<long long>(blockIdx.x) * 2 + sub;
-  const bool active = gblk < static_cast<long long>(a.BH) * nbp;
-  const int blk = active ? static_cast<int>(gblk % nbp) : 0;
-  const int bh = active ? static_cast<int>(gblk / nbp) : 0;
+  const long long gblk = static_cast<long long>(blockIdx.x) * 8 + warp;
+  if (gblk >= static_cast<long long>(a.BH) * nbp) return;   // warp-uniform; no block-wide sync below
+  const int blk = static_cast<int>(gblk % nbp);
+  const int bh = static_cast<int>(gblk / nbp);
   const int b = bh / a.H, h = bh % a.H;
   const int half = lane >> 4;
   const int c8 = (lane & 15) * 8;
   // K smoothing: subtract the channel means before quantising.
   float mu[8] = {0, 0, 0, 0, 0, 0, 0, 0};
   const bool smooth = kSmooth && tensor == 1;
-  if (smooth && active) {
+  if (smooth) {
     const float4* m4 = reinterpret_cast<const float4*>(a.k_mean + static_cast<size_t>(bh) * kHeadDim + c8);
     const float4 m0 = m4[0], m1 = m4[1];
     mu[0] = m0.x; mu[1] = m0.y; mu[2] = m0.z; mu[3] = m0.w;
     mu[4] = m1.x; mu[5] = m1.y; mu[6] = m1.z; mu[7] = m1.w;
   }
-  const int tok0 = blk * 32 + w4 * 8 + half;   // this lane's first token; then +2, +4, +6
+  const int tok0 = blk * 32 + half;   // this lane's tokens: tok0 + 2*it, it = 0..15
   const size_t tok_stride = static_cast<size_t>(a.H) * kHeadDim;
   const uint16_t* src = x + (static_cast<size_t>(b) * S * a.H + h) * kHeadDim + c8;
 
-  uint4 raw[4];
+  uint4 raw[16];
+#pragma unroll
+  for (int it = 0; it < 16; ++it) {
+    const int s = tok0 + 2 * it;
+    raw[it] = s < S ? __ldcs(reinterpret_cast<const uint4*>(src + static_cast<size_t>(s) * tok_stride))
+                    : make_uint4(0, 0, 0, 0);
+  }
   float amax = 0.0f;
 #pragma unroll
-  for (int it = 0; it < 4; ++it) {
-    const int s = tok0 + 2 * it;
-    const bool valid = active && s < S;
-    raw[it] = valid ? __ldcs(reinterpret_cast<const uint4*>(src + static_cast<size_t>(s) * tok_stride))
-                    : make_uint4(0, 0, 0, 0);
+  for (int it = 0; it < 16; ++it) {
     const uint32_t w[4] = {raw[it].x, raw[it].y, raw[it].z, raw[it].w};
     if (smooth) {
+      if (tok0 + 2 * it < S) {
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
-        if (valid)
-          amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w[i]) - mu[2 * i]), fabsf(bf16_hi(w[i]) - mu[2 * i + 1])));
+        for (int i = 0; i < 4; ++i)
+          amax = fmax3(amax, fabsf(bf16_lo(w[i]) - mu[2 * i]), fabsf(bf16_hi(w[i]) - mu[2 * i + 1]));
+      }
     } else {
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
-        amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w[i])), fabsf(bf16_hi(w[i]))));
+      for (int i = 0; i < 4; ++i) amax = fmax3(amax, fabsf(bf16_lo(w[i])), fabsf(bf16_hi(w[i])));
     }
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
-  if (lane == 0) warp_max[warp] = amax;
-  __syncthreads();
-  amax = fmaxf(fmaxf(warp_max[sub * 4], warp_max[sub * 4 + 1]),
-               fmaxf(warp_max[sub * 4 + 2], warp_max[sub * 4 + 3]));
-  if (!active) return;
   const float sc = __fdiv_rn(amax, 127.0f);
   const float rcp = __frcp_rn(sc);
   const bool fast_sc = sc >= 0x1p-125f && sc <= 0x1p125f;
-  if (w4 == 0 && lane == 0 && blk < nb) scale[static_cast<size_t>(bh) * nb + blk] = sc;
+  if (lane == 0 && blk < nb) scale[static_cast<size_t>(bh) * nb + blk] = sc;
 
   CodeT* dst = codes + (static_cast<size_t>(bh) * S_pad + tok0) * kHeadDim + c8;
 #pragma unroll
-  for (int it = 0; it < 4; ++it) {
+  for (int it = 0; it < 16; ++it) {
     const uint32_t w[4] = {raw[it].x, raw[it].y, raw[it].z, raw[it].w};
     float xs[8], c[8];
     const bool valid = tok0 + 2 * it < S;   // rows past the end stay 0 (no -mean)
@@ -392,7 +389,7 @@ __global__ void __launch_bounds__(256) widen_codes_kernel(const int8_t* __restri
 template <typename CodeT>
 cudaError_t launch_qk_quantize(const QKQuantArgs<CodeT>& a, cudaStream_t stream) {
   const long long blocks = static_cast<long long>(a.BH) * (std::max(a.first ? 0 : a.S_pad[0], a.S_pad[1]) / 32);
-  const long long ctas = (blocks + 1) / 2;
+  const long long ctas = (blocks + 7) / 8;
   const dim3 grid(static_cast<unsigned>(ctas), 2 - a.first);
   if (a.k_mean != nullptr)
     qk_quantize_kernel<CodeT, true><<<grid, 256, 0, stream>>>(a);
