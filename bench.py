@@ -388,7 +388,7 @@ def run_ours(args, group, local):
                 "note": "pinned host Q/K/V -> device, sage_attn_fwd, output -> pinned host, every step; "
                         "copies of neighbouring steps overlap compute on separate streams"}
         if e2e_value is not None else {"skipped": "--no-e2e"},
-        "gpu_launches": 4 * K,
+        "gpu_launches": qad.attn_fwd_launches(w.B, w.S, w.H, Skv=w.Skv, smooth_k=args.smooth_k) * K,
         "roofline": {
             "bound": "tensor", "achieved": round(achieved, 1), "peak": round(peak, 1), "unit": "TFLOP/s",
             "frac": round(achieved / peak, 4), "traffic": attention_traffic(),

@@ -249,6 +249,13 @@ extern "C" {
 
 int64_t sage_padded_len(int S) { return S < 1 ? 0 : static_cast<int64_t>(padded_len(S)); }
 
+int sage_attn_fwd_launches(int B, int Sq, int Skv, int H, int smooth_k) {
+  if (B < 1 || Sq < 1 || Skv < 1 || H < 1) return -1;
+  // Q/K quantisation, V maxima, V encoding, attention; K smoothing adds the
+  // channel sums and means.
+  return 4 + (smooth_k ? 2 : 0);
+}
+
 size_t sage_workspace_bytes(int B, int S, int H, int D) {
   if (D != kHeadDim || B < 1 || S < 1 || H < 1 || static_cast<int64_t>(B) * H > INT_MAX || S > (1 << 28))
     return 0;

@@ -35,7 +35,7 @@ EXPORTED = (
     "sage_last_error", "sage_status_string", "sage_set_attention_events",
     "sage_quantize_qkv_noalloc", "sage_attn_fwd_lse", "sage_attn_fwd_cross",
     "sage_debug_fused_q", "sage_attn_fwd_fused_q", "sage_quantize_qkv_smooth_k",
-    "sage_attn_fwd_smooth_k",
+    "sage_attn_fwd_smooth_k", "sage_attn_fwd_launches",
 )
 
 
@@ -66,6 +66,7 @@ def load_library(path: str = LIB_PATH):
         S = ctypes.c_int
         sigs = {
             "sage_padded_len": (ctypes.c_int64, [I]),
+            "sage_attn_fwd_launches": (I, [I, I, I, I, I]),
             "sage_workspace_bytes": (Z, [I, I, I, I]),
             "sage_quantize_qkv": (S, [P, P, P, I, I, I, I, P, P, P, P, P, P, P]),
             "sage_quantize_qkv_noalloc": (S, [P, P, P, I, I, I, I, P, P, P, P, P, P, P]),
@@ -131,6 +132,15 @@ def _check_qkv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor):
 
 def padded_len(S: int) -> int:
     return int(load_library().sage_padded_len(S))
+
+
+def attn_fwd_launches(B: int, Sq: int, H: int, Skv: int | None = None, smooth_k: bool = False) -> int:
+    """Kernels one sage_attn_fwd (or _lse, _cross, _fused_q; _smooth_k with
+    smooth_k) call launches for this shape."""
+    n = int(load_library().sage_attn_fwd_launches(B, Sq, Sq if Skv is None else Skv, H, int(smooth_k)))
+    if n < 0:
+        raise ValueError(f"invalid shape B={B} Sq={Sq} Skv={Skv} H={H}")
+    return n
 
 
 def workspace_bytes(B: int, S: int, H: int, D: int = HEAD_DIM) -> int:
