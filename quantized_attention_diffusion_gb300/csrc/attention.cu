@@ -158,8 +158,7 @@ __device__ __forceinline__ void softmax_p(const float (&a)[kKV], const float (&c
       const float2 x23 = ffma2_bc(a[c + 2], a[c + 3], cb[blk], -bias);
       const float p0 = ex2_approx(x01.x), p1 = ex2_approx(x01.y);
       const float p2 = ex2_approx(x23.x), p3 = ex2_approx(x23.y);
-      pk[blk * 8 + w] =
-          static_cast<uint32_t>(cvt_e4m3x2(p0, p1)) | (static_cast<uint32_t>(cvt_e4m3x2(p2, p3)) << 16);
+      pk[blk * 8 + w] = cvt_e4m3x4(p0, p1, p2, p3);
     }
   }
 }

@@ -281,6 +281,19 @@ __device__ __forceinline__ uint16_t cvt_e4m3x2(float lo, float hi) {
   return r;
 }
 
+// Four E4M3 codes in one word (p0 in the low byte), from two paired
+// conversions written straight into the word's halves.
+__device__ __forceinline__ uint32_t cvt_e4m3x4(float p0, float p1, float p2, float p3) {
+  uint32_t r;
+  asm("{\n\t.reg .b16 l, h;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 l, %2, %1;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 h, %4, %3;\n\t"
+      "mov.b32 %0, {l, h};\n\t}"
+      : "=r"(r)
+      : "f"(p0), "f"(p1), "f"(p2), "f"(p3));
+  return r;
+}
+
 // (a0, a1) * b + c on the packed FP32 pipe: returns {a0*b + c, a1*b + c}.
 __device__ __forceinline__ float2 ffma2_bc(float a0, float a1, float b, float c) {
   float2 r;
