@@ -25,9 +25,6 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
   return t;
 }
 
-__device__ __forceinline__ uint32_t elect_lane0() {
-  return (threadIdx.x & 31u) == 0u;
-}
 
 // ------------------------------------------------------------- mbarrier --
 
@@ -248,12 +245,6 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       : "memory");
 }
 
-// 8 consecutive 32-bit TMEM columns of this thread's lane.
-__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
-               "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
-               : "memory");
-}
 
 __device__ __forceinline__ void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
@@ -345,27 +336,7 @@ __device__ __forceinline__ float2 fsub2v(float2 a, float2 b) {
   return r;
 }
 
-// Two E4M3 codes (low byte first) -> their exact values as f16x2.
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t codes) {
-  uint32_t h2;
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(codes));
-  return h2;
-}
 
-__device__ __forceinline__ uint32_t hadd2(uint32_t a, uint32_t b) {
-  uint32_t r;
-  asm("add.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-  return r;
-}
 
-// acc + lo(h2) + hi(h2), accumulated in fp32.
-__device__ __forceinline__ float add_f32_f16x2(float acc, uint32_t h2) {
-  float r;
-  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\t"
-      "add.rn.f32.f16 %0, lo, %2;\n\tadd.rn.f32.f16 %0, hi, %0;\n\t}"
-      : "=f"(r)
-      : "r"(h2), "f"(acc));
-  return r;
-}
 
 }  // namespace sage
