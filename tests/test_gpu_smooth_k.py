@@ -101,3 +101,30 @@ def test_smooth_k_full_size_sampled_rows():
     got = out.float().cpu().numpy()[rows[:, 0], rows[:, 2], rows[:, 1]]
     err, _ = assert_close_to_oracle(got, f32(ref), ties, w.name)
     print(f"{w.name} smooth_k: max-abs vs oracle {err:.4g}")
+
+
+@pytest.mark.parametrize("name", ["b1_s4096_h24_koffset", "b2_s16384_h24_outlier", "b1_s65536_h24_koffset"])
+def test_smooth_k_accuracy_compared_with_plain(name):
+    """The comparison the pages make for smooth_k (InvokeAI PR #9657,
+    "Summary": it helps on some heads and hurts on outlier heads): the same
+    call with and without K smoothing against unquantized float64 attention
+    on 4 heads x 256 sampled rows of the K-offset (4096 and 65536 tokens) and
+    outlier-channel (2 x 16384) workloads.  Both must keep the accuracy bar
+    (cosine 0.999); the printed cosine and relative L2 are the comparison."""
+    import quantized_attention_diffusion_gb300 as qad
+    from tests.gpu_common import COS_BAR, cosine
+    w = WORKLOADS[name]
+    q, k, v = make_workload(w)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    rows = sample_rows(w.B, w.S, w.H, heads=4, rows_per_head=256, seed=w.seed + 7)
+    rt = torch.from_numpy(rows).long().cuda()
+    exact = oracle.attention_fp64(*[bf16_bits(t) for t in (q, k, v)], w.softmax_scale, rows=rows).ravel()
+    report = []
+    for smooth in (False, True):
+        out = qad.attn_fwd(qd, kd, vd, w.softmax_scale, smooth_k=smooth)
+        got = out[rt[:, 0], rt[:, 2], rt[:, 1]].double().cpu().numpy().ravel()
+        cos = cosine(got, exact)
+        rel = float(np.linalg.norm(got - exact) / np.linalg.norm(exact))
+        report.append(f"smooth_k={smooth}: cosine {cos:.6f} rel-L2 {rel:.4e}")
+        assert cos >= COS_BAR, (name, smooth, cos)
+    print(f"{name}: " + "; ".join(report))
