@@ -66,3 +66,18 @@ def test_fused_q_special_values_bit_exact():
 def test_fused_q_full_size_4096x24_bit_exact():
     qkv, bits = gen(1, 4096, 24, "k_channel_offset", 1)
     _check(qkv, bits[0])
+
+
+def test_fused_q_output_equals_plain_at_bench_size():
+    """B=2 S=16384 H=24 with outlier channels (the benchmark's workload and
+    launch configuration): the in-kernel Q quantisation gives the separate
+    pass's codes, so the two outputs are the same bits."""
+    import quantized_attention_diffusion_gb300 as qad
+    from quantized_attention_diffusion_gb300.workloads import WORKLOADS, make_workload
+    w = WORKLOADS["b2_s16384_h24_outlier"]
+    q, k, v = [t.cuda() for t in make_workload(w)]
+    out_fused = qad.attn_fwd(q, k, v, w.softmax_scale, fused_q=True)
+    out_plain = qad.attn_fwd(q, k, v, w.softmax_scale)
+    torch.cuda.synchronize()
+    diff = out_fused.view(torch.int16) != out_plain.view(torch.int16)
+    assert not diff.any(), f"{int(diff.sum())} outputs differ"
