@@ -208,3 +208,25 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     out = qad.attn_fwd(*[t.cuda() for t in qkv])            # the context is still usable
     _check_output(bf16_out_to_f32(out), *bits, default_scale())
     assert qad.sync_status() == 0
+
+
+def test_repeated_calls_are_bit_identical():
+    """The path is deterministic: the attention kernel has no atomics, and the
+    quantisers' only atomics (an fp32-bit max per V channel, 64-bit integer
+    sums of K for smoothing) do not depend on their order.  Two calls at the
+    benchmark's size, one on a second stream, give the same bits."""
+    import quantized_attention_diffusion_gb300 as qad
+    from quantized_attention_diffusion_gb300.workloads import WORKLOADS, make_workload
+    w = WORKLOADS["b2_s16384_h24_outlier"]
+    q, k, v = [t.cuda() for t in make_workload(w)]
+    a = qad.attn_fwd(q, k, v, w.softmax_scale)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        b = qad.attn_fwd(q, k, v, w.softmax_scale)
+        s1 = qad.attn_fwd(q, k, v, w.softmax_scale, smooth_k=True)
+    torch.cuda.synchronize()
+    s2 = qad.attn_fwd(q, k, v, w.softmax_scale, smooth_k=True)
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    assert torch.equal(s1.view(torch.int16), s2.view(torch.int16))
