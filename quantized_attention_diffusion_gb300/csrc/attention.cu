@@ -462,17 +462,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       float a[kKV];
       {
-        uint32_t r0[32], r1[32], r2[32];
-        tmem_ld32(tS, r0);
-        tmem_ld32(tS + 32, r1);
+        uint32_t r01[64], r2[32];
+        tmem_ld64(tS, r01);
         tmem_ld32(tS + 64, r2);
         tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          a[i] = __uint_as_float(r0[i]);
-          a[32 + i] = __uint_as_float(r1[i]);
-          a[64 + i] = __uint_as_float(r2[i]);
-        }
+        for (int i = 0; i < 64; ++i) a[i] = __uint_as_float(r01[i]);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) a[64 + i] = __uint_as_float(r2[i]);
       }
       // The scores are in registers: S_t may take the next tile's scores.
       tc_fence_before();
