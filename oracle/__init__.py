@@ -71,13 +71,17 @@ def _load():
         lib.oracle_qk_int32.argtypes = [P, P, I, I, I, I, I, P]
         lib.oracle_attend_rows.restype = I
         lib.oracle_attend_rows.argtypes = [P, P, P, P, P, P, I, I, I, I, I,
-                                           ctypes.c_float, I, P, ctypes.c_int64, P, P, P, P]
+                                           ctypes.c_float, I, I, P, ctypes.c_int64, P, P, P, P]
         lib.oracle_attend_rows_cross.restype = I
         lib.oracle_attend_rows_cross.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, I,
-                                                 ctypes.c_float, I, P, ctypes.c_int64, P, P, P, P]
+                                                 ctypes.c_float, I, I, P, ctypes.c_int64, P, P,
+                                                 P, P]
         lib.oracle_attend_row_debug.restype = I
         lib.oracle_attend_row_debug.argtypes = [P, P, P, P, P, P, I, I, I, I, I,
-                                                ctypes.c_float, I, I, I, I, P, P, P, P]
+                                                ctypes.c_float, I, I, I, I, I, P, P, P, P]
+        lib.oracle_requant_bound.restype = I
+        lib.oracle_requant_bound.argtypes = [P, P, P, P, I, I, I, I, I, I, I, ctypes.c_float, I,
+                                             P, ctypes.c_int64, P]
         lib.oracle_num_threads.restype = I
         _lib = lib
         return lib
@@ -153,6 +157,13 @@ def qk_int32(q_codes: np.ndarray, k_codes: np.ndarray, S: int) -> np.ndarray:
 
 # --------------------------------------------------------------- attention --
 
+#: KV tile of the online softmax (reading R7).  The pages fix none; 96 keys
+#: (three K blocks) follows the CUDA kernel's tile.  0 selects one tile of
+#: all keys: the exact two-pass softmax.
+KV_TILE = 96
+TWO_PASS = 0
+
+
 def all_rows(B: int, S: int, H: int) -> np.ndarray:
     """Every (b, h, i) query row, in [B, S, H] output order."""
     b, s, h = np.meshgrid(np.arange(B), np.arange(S), np.arange(H), indexing="ij")
@@ -160,7 +171,8 @@ def all_rows(B: int, S: int, H: int) -> np.ndarray:
 
 
 def attend_rows(quant, S: int, softmax_scale: float, rows: np.ndarray, l_mode: int = 0,
-                return_ties: bool = False, return_lse: bool = False, Skv: int | None = None):
+                return_ties: bool = False, return_lse: bool = False, Skv: int | None = None,
+                kv_tile: int = KV_TILE):
     """Attention output for selected query rows from quantised operands.
 
     quant = (q_codes, q_scale, k_codes, k_scale, vt_codes, v_scale) in the
@@ -171,7 +183,8 @@ def attend_rows(quant, S: int, softmax_scale: float, rows: np.ndarray, l_mode: i
     return_lse also each row's log-sum-exp (reading R13) and its tie bound
     (two float64 [n]), appended in that order.  S is the number of query
     rows; Skv (default S) the number of keys and values (cross-attention,
-    reading R14).
+    reading R14).  kv_tile: the online softmax's KV tile (reading R7; 0 or
+    ``TWO_PASS`` for one tile of all keys).
     """
     qc, qs, kc, ks, vt, vs = [np.ascontiguousarray(a) for a in quant]
     B, H, Sp, D = qc.shape
@@ -184,7 +197,7 @@ def attend_rows(quant, S: int, softmax_scale: float, rows: np.ndarray, l_mode: i
     lse_ties = np.zeros(rows.shape[0], dtype=np.float64)
     rc = _load().oracle_attend_rows_cross(_ptr(qc), _ptr(qs), _ptr(kc), _ptr(ks), _ptr(vt),
                                           _ptr(vs), B, S, Skv, H, D, Sp, Skv_pad,
-                                          float(softmax_scale), int(l_mode), _ptr(rows),
+                                          float(softmax_scale), int(l_mode), int(kv_tile), _ptr(rows),
                                           rows.shape[0], _ptr(out), _ptr(ties), _ptr(lse),
                                           _ptr(lse_ties))
     if rc != 0:
@@ -198,7 +211,7 @@ def attend_rows(quant, S: int, softmax_scale: float, rows: np.ndarray, l_mode: i
 
 
 def attend_row_debug(quant, S: int, softmax_scale: float, b: int, h: int, i: int,
-                     l_mode: int = 0):
+                     l_mode: int = 0, kv_tile: int = KV_TILE):
     """One row with its FP8 P codes and normaliser L: (out bf16 [D], codes [S], L)."""
     qc, qs, kc, ks, vt, vs = [np.ascontiguousarray(a) for a in quant]
     B, H, Sp, D = qc.shape
@@ -208,7 +221,7 @@ def attend_row_debug(quant, S: int, softmax_scale: float, b: int, h: int, i: int
     tie = ctypes.c_double(0.0)
     rc = _load().oracle_attend_row_debug(_ptr(qc), _ptr(qs), _ptr(kc), _ptr(ks), _ptr(vt),
                                          _ptr(vs), B, S, H, D, Sp, float(softmax_scale),
-                                         int(l_mode), b, h, i, _ptr(out), _ptr(pc),
+                                         int(l_mode), int(kv_tile), b, h, i, _ptr(out), _ptr(pc),
                                          ctypes.byref(L), ctypes.byref(tie))
     if rc != 0:
         raise MemoryError("oracle_attend_row_debug failed to allocate")
@@ -239,7 +252,7 @@ def quantize(q: np.ndarray, k: np.ndarray, v: np.ndarray, smooth_k: bool = False
 
 def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, softmax_scale: float,
               rows: np.ndarray | None = None, l_mode: int = 0, return_ties: bool = False,
-              smooth_k: bool = False):
+              smooth_k: bool = False, kv_tile: int = KV_TILE):
     """Whole quantize-then-attend path from bf16 bits.
 
     rows None: full output bf16 bits [B,S,H,D] (ties [B,S,H]); otherwise
@@ -249,8 +262,39 @@ def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, softmax_scale: float,
     Skv = k.shape[1]
     quant = quantize(q, k, v, smooth_k=smooth_k)
     if rows is None:
-        out, ties = attend_rows(quant, S, softmax_scale, all_rows(B, S, H), l_mode, True, Skv=Skv)
+        out, ties = attend_rows(quant, S, softmax_scale, all_rows(B, S, H), l_mode, True, Skv=Skv,
+                                kv_tile=kv_tile)
         out, ties = out.reshape(B, S, H, D), ties.reshape(B, S, H)
     else:
-        out, ties = attend_rows(quant, S, softmax_scale, rows, l_mode, True, Skv=Skv)
+        out, ties = attend_rows(quant, S, softmax_scale, rows, l_mode, True, Skv=Skv,
+                                kv_tile=kv_tile)
     return (out, ties) if return_ties else out
+
+
+# ------------------------------------------------- tiling bound (R16) --
+
+def requant_bound(quant, S: int, softmax_scale: float, rows: np.ndarray,
+                  kv_tile: int = KV_TILE, Skv: int | None = None) -> np.ndarray:
+    """Per row, the factor G of reading R16: the output with KV tiles of
+    ``kv_tile`` keys and the two-pass output differ by at most
+    ``v_spread(quant)[b, h, d] * G`` in channel d (plus one BF16 ulp).
+    G is computed from the exact scores alone.  Returns float64 [n]."""
+    qc, qs, kc, ks, _, _ = [np.ascontiguousarray(a) for a in quant]
+    B, H, Sp, D = qc.shape
+    Skv = S if Skv is None else int(Skv)
+    rows = np.ascontiguousarray(rows, dtype=np.int32).reshape(-1, 3)
+    G = np.empty(rows.shape[0], dtype=np.float64)
+    rc = _load().oracle_requant_bound(_ptr(qc), _ptr(qs), _ptr(kc), _ptr(ks), B, S, Skv, H, D, Sp,
+                                      kc.shape[2], float(softmax_scale), int(kv_tile), _ptr(rows),
+                                      rows.shape[0], _ptr(G))
+    if rc != 0:
+        raise MemoryError("oracle_requant_bound failed to allocate")
+    return G
+
+
+def v_spread(quant, Skv: int) -> np.ndarray:
+    """max - min over the Skv tokens of the dequantised V, per (b, h, d):
+    float64 [B, H, D] (the spread_d of reading R16)."""
+    _, _, _, _, vt, vs = quant
+    dec = e4m3_decode(vt[..., :int(Skv)]) * vs.astype(np.float64)[..., None]
+    return dec.max(axis=-1) - dec.min(axis=-1)

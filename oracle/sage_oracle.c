@@ -35,13 +35,17 @@
  *      so that exp(s_j - s_k) = 2^(x_j - x_k) with s = acc * sq * sk *
  *      softmax_scale.  The kernel takes the FP8 decisions of R8 from these
  *      same fp32 values, so both sides decide every P code in one precision.
- *  R7  online softmax in FP32 over KV tiles of 96 keys (keys [96t, 96t+96)
- *      that exist; 96 = three K blocks): the running max m_t = max(m_{t-1}, max_{j in
- *      t} x_j) (m_{-1} = -inf); bias_t = fl(m_t - LOG2_448) with LOG2_448 =
+ *  R7  online softmax in FP32 over KV tiles of T keys (keys [T t, T t + T)
+ *      that exist): the running max m_t = max(m_{t-1}, max_{j in t} x_j)
+ *      (m_{-1} = -inf); bias_t = fl(m_t - LOG2_448) with LOG2_448 =
  *      fp32(log2 448); p_j = fp32(2^fmaf(acc_j, cb_j, -bias_t)) (2^ in double,
  *      rounded once), so p_j <= 448 is 448 * exp(s_j - running max);
  *      alpha_t = fp32(2^fl(m_{t-1} - m_t)) rescales what was accumulated
- *      (alpha_0 = 0).
+ *      (alpha_0 = 0).  The pages fix no tile: T is an argument.  T = 96 (three
+ *      K blocks) follows the CUDA kernel's tile and is the default the parity
+ *      tests compare against bit for bit; T = 0 means one tile holding every
+ *      key, which is the exact two-pass softmax (m = the row's true max, every
+ *      p_j = 448 exp(s_j - m), no rescale).  The bound of R16 links the two.
  *  R8  P to FP8 per tile, against the running max: code_j = e4m3(p_j).
  *  R9  normaliser L = alpha_t * L + sum_{j in t} dec(code_j) (the applied
  *      quantised weights, in double); l_mode = 1 selects the alternative
@@ -66,6 +70,23 @@
  *  R14 (cross-attention) Q may have Sq rows and K, V S != Sq rows: each is
  *      quantised over its own 32-row blocks (Q, K) or its own tokens (V);
  *      every step above runs over the S keys unchanged.
+ *
+ *  R16 (bound between tilings)  For a tile T and the two-pass form (T = 0)
+ *      the scores x_j, the final max m and every fp32 step are the same; a key
+ *      in a tile at or after the one that holds the row max gets the same p_j,
+ *      the same code and no later rescale (alpha = 2^0 = 1) in both, so only
+ *      the keys of earlier tiles ("early" keys) weigh differently.  With
+ *      y_j = 2^(acc_j cb_j - m + LOG2_448) exact, each applied weight w_j
+ *      (code value times the product of later alphas) satisfies
+ *      |w_j - y_j| <= b_j: the E4M3 rounding error of p_j in its tile's units
+ *      (2^-4 p relative at or above 2^-6, at most min(p, 2^-10) below) scaled
+ *      back by 2^(m_t - m), plus a relative slack eta_j for the fp32 roundings
+ *      (bias, fma, 2^x, alphas).  Since o(w) - o(w') = sum_j (w_j - w'_j)
+ *      (v_j - o(w')) / sum_j w_j for any two weightings,
+ *        |out_T[d] - out_0[d]| <= spread_d * G,
+ *        G = sum_{j early} (b_j(T) + b_j(0)) / (sum_j y_j - sum_j b_j(T)),
+ *      with spread_d = max_j v_jd - min_j v_jd of the dequantised V, plus one
+ *      BF16 ulp for the two final roundings.  oracle_requant_bound returns G.
  *
  *  Tie bound.  A P code whose p_j lies within 2^-19 (relative) of a
  *  rounding midpoint of the E4M3 grid is a tie: an implementation whose 2^x
@@ -231,7 +252,7 @@ int oracle_qk_int32(const int8_t *q, const int8_t *k, int B, int S, int H,
 /* The fp32 value nearest log2(e), and fp32(log2(448)). */
 #define ORACLE_L2E 1.44269502162933349609375f
 #define ORACLE_LOG2_448 8.80735492706298828125f
-#define ORACLE_KV_TILE 96
+#define ORACLE_KV_TILE 96   /* default T of R7: the CUDA kernel's tile */
 #define ORACLE_TIE_REL 1.9073486328125e-06 /* 2^-19 */
 
 /* Distance of an E4M3 code's value to the other side of the nearest rounding
@@ -260,11 +281,12 @@ static double tie_step(float y, uint8_t code) {
  * not NULL it receives the S FP8 codes of P (each against the running max of
  * its tile) and *L_out the normaliser; *tie_out (if not NULL) the row's tie
  * bound.  vdec is this head's decoded V, [S][D] floats (exact); acc is
- * scratch for one tile's integer scores.  R6..R11. */
+ * scratch for one tile's integer scores (S entries).  kv_tile is T of R7
+ * (0: one tile of all S keys, the two-pass form).  R6..R11. */
 static void attend_row(const int8_t *q, const float *qs, const int8_t *k,
                        const float *ks, const float *vdec, const float *vs,
                        int b, int h, int i, int Sq, int S, int H, int D, int Sq_pad, int S_pad,
-                       float softmax_scale, int l_mode, float *sbuf,
+                       float softmax_scale, int l_mode, int kv_tile, float *sbuf,
                        int32_t *acc, uint8_t *cbuf, double *obuf, uint16_t *out_row,
                        uint8_t *pcodes, double *L_out, double *tie_out,
                        double *lse_out, double *lse_tie_out) {
@@ -277,8 +299,9 @@ static void attend_row(const int8_t *q, const float *qs, const int8_t *k,
     double L = 0.0, T = 0.0;
     float m_run = -INFINITY;
     for (int d = 0; d < D; ++d) obuf[d] = 0.0;
-    for (int j0 = 0; j0 < S; j0 += ORACLE_KV_TILE) {
-        int j1 = j0 + ORACLE_KV_TILE < S ? j0 + ORACLE_KV_TILE : S;
+    int tile = (kv_tile <= 0 || kv_tile > S) ? S : kv_tile;   /* R7: 0 = one tile */
+    for (int j0 = 0; j0 < S; j0 += tile) {
+        int j1 = j0 + tile < S ? j0 + tile : S;
         /* integer scores (R5) and their base-2 values (R6); sbuf keeps cb_j */
         float m_tile = -INFINITY;
         for (int j = j0; j < j1; ++j) {
@@ -381,15 +404,15 @@ static void decode_v_head(const uint8_t *vt, int b, int h, int S, int H, int D,
  * out: bf16 [n, D] in the order of rows.  Every (b, h) named in rows must
  * appear; heads are decoded once.  ties (may be NULL): double [n], each
  * row's tie bound.  lse, lse_ties (may be NULL): double [n], each row's
- * log-sum-exp (R13) and its tie bound.  Returns 0, or -1 on allocation
- * failure.  [I15014] bullets 1-2, [P15060] ("no LSE"): the kernel contract's
+ * log-sum-exp (R13) and its tie bound.  kv_tile: T of R7 (0: two-pass).
+ * Returns 0, or -1 on allocation failure.  [I15014] bullets 1-2, [P15060] ("no LSE"): the kernel contract's
  * output is the normalised attention; the LSE is the optional extra output. */
 int oracle_attend_rows_cross(const int8_t *q, const float *qs, const int8_t *k,
                              const float *ks, const uint8_t *vt, const float *vs,
                              int B, int Sq, int S, int H, int D, int Sq_pad, int S_pad,
-                             float softmax_scale, int l_mode, const int32_t *rows,
-                             int64_t n, uint16_t *out, double *ties, double *lse,
-                             double *lse_ties) {
+                             float softmax_scale, int l_mode, int kv_tile,
+                             const int32_t *rows, int64_t n, uint16_t *out, double *ties,
+                             double *lse, double *lse_ties) {
     /* decode the heads in use */
     int nheads = B * H;
     float **vdec = (float **)calloc((size_t)nheads, sizeof(float *));
@@ -409,7 +432,7 @@ int oracle_attend_rows_cross(const int8_t *q, const float *qs, const int8_t *k,
 #pragma omp parallel
         {
             float *sbuf = (float *)malloc((size_t)S * sizeof(float));
-            int32_t *abuf = (int32_t *)malloc(ORACLE_KV_TILE * sizeof(int32_t));
+            int32_t *abuf = (int32_t *)malloc((size_t)S * sizeof(int32_t));
             uint8_t *cbuf = (uint8_t *)malloc((size_t)S);
             double *obuf = (double *)malloc((size_t)D * sizeof(double));
             if (!sbuf || !abuf || !cbuf || !obuf) {
@@ -420,7 +443,8 @@ int oracle_attend_rows_cross(const int8_t *q, const float *qs, const int8_t *k,
                 for (int64_t r = 0; r < n; ++r) {
                     int b = rows[3 * r], h = rows[3 * r + 1], i = rows[3 * r + 2];
                     attend_row(q, qs, k, ks, vdec[b * H + h], vs, b, h, i, Sq, S, H, D,
-                               Sq_pad, S_pad, softmax_scale, l_mode, sbuf, abuf, cbuf, obuf,
+                               Sq_pad, S_pad, softmax_scale, l_mode, kv_tile, sbuf, abuf,
+                               cbuf, obuf,
                                out + (size_t)r * D, NULL, NULL, ties ? ties + r : NULL,
                                lse ? lse + r : NULL, lse_ties ? lse_ties + r : NULL);
                 }
@@ -437,11 +461,12 @@ int oracle_attend_rows_cross(const int8_t *q, const float *qs, const int8_t *k,
 int oracle_attend_rows(const int8_t *q, const float *qs, const int8_t *k,
                        const float *ks, const uint8_t *vt, const float *vs,
                        int B, int S, int H, int D, int S_pad,
-                       float softmax_scale, int l_mode, const int32_t *rows,
+                       float softmax_scale, int l_mode, int kv_tile, const int32_t *rows,
                        int64_t n, uint16_t *out, double *ties, double *lse,
                        double *lse_ties) {
     return oracle_attend_rows_cross(q, qs, k, ks, vt, vs, B, S, S, H, D, S_pad, S_pad,
-                                    softmax_scale, l_mode, rows, n, out, ties, lse, lse_ties);
+                                    softmax_scale, l_mode, kv_tile, rows, n, out, ties, lse,
+                                    lse_ties);
 }
 
 /* Single row with its FP8 P codes and normaliser exposed (for the pins on
@@ -449,24 +474,104 @@ int oracle_attend_rows(const int8_t *q, const float *qs, const int8_t *k,
 int oracle_attend_row_debug(const int8_t *q, const float *qs, const int8_t *k,
                             const float *ks, const uint8_t *vt, const float *vs,
                             int B, int S, int H, int D, int S_pad,
-                            float softmax_scale, int l_mode, int b, int h, int i,
-                            uint16_t *out_row, uint8_t *pcodes, double *L_out,
+                            float softmax_scale, int l_mode, int kv_tile, int b, int h,
+                            int i, uint16_t *out_row, uint8_t *pcodes, double *L_out,
                             double *tie_out) {
     (void)B;
     float *vdec = (float *)malloc((size_t)S * D * sizeof(float));
     float *sbuf = (float *)malloc((size_t)S * sizeof(float));
-    int32_t *abuf = (int32_t *)malloc(ORACLE_KV_TILE * sizeof(int32_t));
+    int32_t *abuf = (int32_t *)malloc((size_t)S * sizeof(int32_t));
     uint8_t *cbuf = (uint8_t *)malloc((size_t)S);
     double *obuf = (double *)malloc((size_t)D * sizeof(double));
     int rc = -1;
     if (vdec && sbuf && abuf && cbuf && obuf) {
         decode_v_head(vt, b, h, S, H, D, S_pad, vdec);
         attend_row(q, qs, k, ks, vdec, vs, b, h, i, S, S, H, D, S_pad, S_pad, softmax_scale,
-                   l_mode, sbuf, abuf, cbuf, obuf, out_row, pcodes, L_out, tie_out, NULL, NULL);
+                   l_mode, kv_tile, sbuf, abuf, cbuf, obuf, out_row, pcodes, L_out, tie_out,
+                   NULL, NULL);
         rc = 0;
     }
     free(vdec); free(sbuf); free(abuf); free(cbuf); free(obuf);
     return rc;
+}
+
+/* Bound on |dec(e4m3(p)) - p| for p >= 0 (R3): half a step, 2^-4 p, in the
+ * normal range (p >= 2^-6, saturation at 448 included); below it half the
+ * subnormal quantum, 2^-10, or p itself where p rounds to zero. */
+static double e4m3_err_bound(double p) {
+    if (p >= 0x1p-6) return 0x1p-4 * p;
+    return p < 0x1p-10 ? p : 0x1p-10;
+}
+
+/* R16: per query row, G with |out_T[d] - out_0[d]| <= spread_d * G (plus one
+ * BF16 ulp), where out_T is the output with KV tiles of kv_tile keys and
+ * out_0 the two-pass output.  Operands as oracle_attend_rows_cross; G: double
+ * [n].  Every term is computed from the exact scores, not from either
+ * output.  Returns 0, or -1 on allocation failure. */
+int oracle_requant_bound(const int8_t *q, const float *qs, const int8_t *k,
+                         const float *ks, int B, int Sq, int S, int H, int D, int Sq_pad,
+                         int S_pad, float softmax_scale, int kv_tile, const int32_t *rows,
+                         int64_t n, double *G) {
+    (void)B;
+    int fail = 0;
+    int tile = (kv_tile <= 0 || kv_tile > S) ? S : kv_tile;
+    int n_tiles = (S + tile - 1) / tile;
+    int nb = (S + 31) / 32, nbq = (Sq + 31) / 32;
+#pragma omp parallel
+    {
+        int32_t *acc = (int32_t *)malloc((size_t)S * sizeof(int32_t));
+        float *cb = (float *)malloc((size_t)S * sizeof(float));
+        float *mt = (float *)malloc((size_t)n_tiles * sizeof(float));
+        if (!acc || !cb || !mt) {
+#pragma omp atomic write
+            fail = 1;
+        } else {
+#pragma omp for schedule(dynamic, 4)
+            for (int64_t r = 0; r < n; ++r) {
+                int b = rows[3 * r], h = rows[3 * r + 1], i = rows[3 * r + 2];
+                const int8_t *qi = q + (((size_t)b * H + h) * Sq_pad + i) * D;
+                float c_row = qs[((size_t)b * H + h) * nbq + i / 32] * (softmax_scale * ORACLE_L2E);
+                /* scores of R6 and the running max of R7 at the end of each tile */
+                float m = -INFINITY;
+                for (int j = 0; j < S; ++j) {
+                    const int8_t *kj = k + (((size_t)b * H + h) * S_pad + j) * D;
+                    int32_t a = 0;
+                    for (int c = 0; c < D; ++c) a += (int32_t)qi[c] * (int32_t)kj[c];
+                    acc[j] = a;
+                    cb[j] = c_row * ks[((size_t)b * H + h) * nb + j / 32];
+                    float x = (float)a * cb[j];
+                    if (x > m) m = x;
+                    if ((j + 1) % tile == 0 || j == S - 1) mt[j / tile] = m;
+                }
+                int t_star = 0;
+                while (mt[t_star] != m) ++t_star;
+                double sum_y = 0.0, sum_b = 0.0, early = 0.0;
+                for (int j = 0; j < S; ++j) {
+                    int t = j / tile;
+                    double prod = (double)acc[j] * (double)cb[j];   /* exact */
+                    double x = fabs((double)((float)acc[j] * cb[j]));
+                    double y = exp2(prod - (double)m + (double)ORACLE_LOG2_448);
+                    /* relative slack of the fp32 steps: the bias, the fma and the
+                     * rounding of 2^x (each <= 2^-24 of its magnitude), and for
+                     * the tiled form the n_tiles alphas and their arguments */
+                    double eta0 = 0x1p-23 * (2.0 + x + 2.0 * (fabs((double)m) + 9.0));
+                    double eta = 0x1p-23 * (2.0 + x + 2.0 * (fabs((double)mt[t]) + 9.0) + n_tiles +
+                                            ((double)m - (double)mt[t]));
+                    double y_tile = exp2(prod - (double)mt[t] + (double)ORACLE_LOG2_448);
+                    double back = exp2((double)mt[t] - (double)m);   /* <= 1 */
+                    double b_t = e4m3_err_bound(y_tile * (1.0 + eta)) * (1.0 + eta) * back + 3.0 * eta * y;
+                    double b_0 = e4m3_err_bound(y * (1.0 + eta0)) * (1.0 + eta0) + 3.0 * eta0 * y;
+                    sum_y += y;
+                    sum_b += b_t;
+                    if (t < t_star) early += b_t + b_0;
+                }
+                double den = sum_y - sum_b;
+                G[r] = early == 0.0 ? 0.0 : (den > 0.0 ? early / den : INFINITY);
+            }
+        }
+        free(acc); free(cb); free(mt);
+    }
+    return fail ? -1 : 0;
 }
 
 /* Threads the OpenMP runtime will use (for the benchmark's core count). */
