@@ -250,6 +250,52 @@ sage_status sage_debug_qk_int32(const int8_t* q_i8, const float* q_scale, const 
                                 void* stream);
 
 /*
+ * sage_debug_staging_codes -- test entry: the Q/K quantisation exactly as
+ * sage_attn_fwd runs it before the attention kernel (the same launch), into
+ * caller buffers.  The codes are the INT8 values of sage_quantize_qkv stored
+ * as fp16 (the tensor-core operand type of QK^T; every code is an integer in
+ * [-127, 127], exact in fp16).  Passage: the issue's contract bullet "Q/K are
+ * quantized per 32-row block".
+ *
+ *   q, k       in : bf16 [B, S, H, D]
+ *   q16, k16   out: fp16 [B, H, S_pad, D]; rows >= S are 0
+ *   q_scale, k_scale out: fp32 [B, H, nb], as sage_quantize_qkv
+ * Errors: INVALID_ARG, UNSUPPORTED, MISALIGNED, CUDA.
+ */
+sage_status sage_debug_staging_codes(const void* q, const void* k, int B, int S, int H, int D, void* q16,
+                                     float* q_scale, void* k16, float* k_scale, void* stream);
+
+/* Fault sites of sage_debug_inject_fault. */
+enum {
+  SAGE_FAULT_NONE = 0,          /* disarm */
+  SAGE_FAULT_POOL_ALLOC = 1,    /* a workspace / scratch allocation from the library's pool */
+  SAGE_FAULT_QUANT_LAUNCH = 2,  /* the Q/K quantisation launch of the attention entry points */
+  SAGE_FAULT_ATTN_LAUNCH = 3    /* the attention kernel launch */
+};
+
+/*
+ * sage_debug_inject_fault -- host-side fault injection for tests (no
+ * counterpart on the pages; off by default).  Arms one site: the site's
+ * (skip+1)-th next event, in any thread, fails without doing its work (no
+ * allocation, no launch) and reports what a real failure there reports --
+ * SAGE_ERR_NO_MEMORY for the pool, SAGE_ERR_CUDA for a launch -- with
+ * "injected fault" in sage_last_error(); then the hook disarms.  Work the
+ * call had already enqueued stays valid, and its workspace is released in
+ * stream order as on every other failure.  Nothing faults on the device, and
+ * the CUDA context stays usable.  Returns INVALID_ARG for an unknown site or
+ * a negative skip.
+ */
+sage_status sage_debug_inject_fault(int site, int skip);
+
+/*
+ * sage_debug_pool_state -- test query (no counterpart on the pages): whether
+ * this library has created its private stream-ordered memory pool on the
+ * current device (*created, 0 or 1), and the bytes currently allocated from
+ * it (*used_bytes; 0 if none).  Host pointers.  Errors: INVALID_ARG, CUDA.
+ */
+sage_status sage_debug_pool_state(int* created, uint64_t* used_bytes);
+
+/*
  * sage_debug_wait_timeout -- test entry for failure detection without a GPU
  * fault: launches one warp that waits on an mbarrier nothing arrives on,
  * with a limit of timeout_ns (1..10^10).  The wait gives up, records

@@ -28,16 +28,22 @@ constexpr size_t kScratchWords = static_cast<size_t>(kMaxBH) * sage::kHeadDim;
 // The scratch: per-(batch*head, channel) |V| maxima as fp32 bit patterns.
 static __device__ __align__(256) uint32_t g_vmax_scratch[kScratchWords];
 
+constexpr int kMaxDevices = 64;
 std::mutex g_mu;
-uint32_t* g_scratch_addr[64] = {};     // device address of the array, per device
+uint32_t* g_scratch_addr[kMaxDevices] = {};   // device address of the array, per device
 
 // Looks up (once per device, with that device current) the device address of
 // g_vmax_scratch.  Returns nullptr and records the error text on failure.
 uint32_t* scratch_for_current_device() {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess || dev < 0 || dev >= 64) {
+  if (e != cudaSuccess) {
     sage::set_last_error("cudaGetDevice failed: %s", cudaGetErrorString(e));
+    return nullptr;
+  }
+  if (dev < 0 || dev >= kMaxDevices) {
+    sage::set_last_error("device index %d exceeds the %d-device table of sage_quantize_qkv_noalloc", dev,
+                         kMaxDevices);
     return nullptr;
   }
   std::lock_guard<std::mutex> lk(g_mu);

@@ -93,16 +93,42 @@ T* at(void* base, size_t off) {
   return reinterpret_cast<T*>(static_cast<uint8_t*>(base) + off);
 }
 
+// Host-only fault injection (a test hook, off by default): when armed for a
+// site, the site's skip-th next event reports a failure without doing the
+// work (no allocation, no launch), and the hook disarms.  Nothing faults on
+// the device.
+std::atomic<int> g_fault_site{0};
+std::atomic<int> g_fault_skip{0};
+
+bool fault_fires(int site) {
+  if (g_fault_site.load(std::memory_order_relaxed) != site) return false;
+  if (g_fault_skip.fetch_sub(1, std::memory_order_relaxed) > 0) return false;
+  g_fault_site.store(0, std::memory_order_relaxed);
+  return true;
+}
+
 // One private stream-ordered pool per device; memory is kept by the pool
 // (release threshold = max) so steady-state calls do not go to the driver.
+// A pool is published in g_pools only once its release threshold is set.
+constexpr int kMaxDevices = 64;
 std::mutex g_pool_mu;
-cudaMemPool_t g_pools[64] = {};
+cudaMemPool_t g_pools[kMaxDevices] = {};
 
-cudaError_t pool_alloc(void** ptr, size_t bytes, cudaStream_t stream) {
+sage_status current_device(int* dev) {
+  cudaError_t e = cudaGetDevice(dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (*dev < 0 || *dev >= kMaxDevices)
+    return fail(SAGE_ERR_CUDA, "device index %d exceeds this library's %d-device table", *dev, kMaxDevices);
+  return SAGE_OK;
+}
+
+// `bytes` of stream-ordered scratch for `what` on the current device.
+sage_status pool_alloc(void** ptr, size_t bytes, cudaStream_t stream, const char* what) {
+  if (fault_fires(SAGE_FAULT_POOL_ALLOC))
+    return fail(SAGE_ERR_NO_MEMORY, "%s allocation of %zu bytes failed: injected fault", what, bytes);
   int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  sage_status s = current_device(&dev);
+  if (s != SAGE_OK) return s;
   cudaMemPool_t pool;
   {
     std::lock_guard<std::mutex> lk(g_pool_mu);
@@ -112,18 +138,65 @@ cudaError_t pool_alloc(void** ptr, size_t bytes, cudaStream_t stream) {
       props.allocType = cudaMemAllocationTypePinned;
       props.location.type = cudaMemLocationTypeDevice;
       props.location.id = dev;
-      e = cudaMemPoolCreate(&g_pools[dev], &props);
-      if (e != cudaSuccess) return e;
+      cudaMemPool_t fresh = nullptr;
+      cudaError_t e = cudaMemPoolCreate(&fresh, &props);
+      if (e != cudaSuccess) return cuda_fail(e, "memory pool creation");
       uint64_t thr = UINT64_MAX;
-      e = cudaMemPoolSetAttribute(g_pools[dev], cudaMemPoolAttrReleaseThreshold, &thr);
-      if (e != cudaSuccess) return e;
+      e = cudaMemPoolSetAttribute(fresh, cudaMemPoolAttrReleaseThreshold, &thr);
+      if (e != cudaSuccess) {
+        (void)cudaMemPoolDestroy(fresh);
+        return cuda_fail(e, "memory pool release threshold");
+      }
+      g_pools[dev] = fresh;
     }
     pool = g_pools[dev];
   }
-  return cudaMallocFromPoolAsync(ptr, bytes, pool, stream);
+  cudaError_t e = cudaMallocFromPoolAsync(ptr, bytes, pool, stream);
+  if (e != cudaSuccess) {
+    // An out-of-memory result is not sticky, but the runtime keeps it as the
+    // thread's last error: clear it so that it is not reported by a later
+    // call's launch check.
+    (void)cudaGetLastError();
+    return fail(SAGE_ERR_NO_MEMORY, "%s allocation of %zu bytes failed: %s", what, bytes, cudaGetErrorString(e));
+  }
+  return SAGE_OK;
+}
+
+// Allocate `bytes` of workspace from the pool, run `body(ws)`, release the
+// workspace in stream order whatever body returned.
+template <typename Body>
+sage_status with_pool_workspace(size_t bytes, cudaStream_t st, Body body) {
+  void* ws = nullptr;
+  sage_status s = pool_alloc(&ws, bytes, st, "workspace");
+  if (s != SAGE_OK) return s;
+  s = body(ws);
+  cudaError_t e = cudaFreeAsync(ws, st);
+  if (s != SAGE_OK) return s;
+  if (e != cudaSuccess) return cuda_fail(e, "workspace release");
+  return SAGE_OK;
 }
 
 uint64_t timeout_ns() { return g_timeout_ns.load(std::memory_order_relaxed); }
+
+// Arguments of the Q/K quantisation that feeds the attention kernel: integer
+// codes stored as fp16 (the MMA operand type), [B, H, S_pad, 128].  With
+// k_only, Q is left to the attention kernel; k_mean selects K smoothing.
+QKQuantArgs<__half> staging_args(const void* q, const void* k, int B, int Sq, int Sk, int H, __half* q16,
+                                 float* q_scale, __half* k16, float* k_scale, bool k_only, const float* k_mean) {
+  QKQuantArgs<__half> qa;
+  qa.q = static_cast<const uint16_t*>(q);
+  qa.k = static_cast<const uint16_t*>(k);
+  qa.q_codes = q16;
+  qa.k_codes = k16;
+  qa.q_scale = q_scale;
+  qa.k_scale = k_scale;
+  qa.BH = B * H;
+  qa.H = H;
+  qa.set_lengths(Sq, Sk);
+  qa.first = k_only ? 1 : 0;
+  qa.k_mean = k_mean;
+  return qa;
+}
 
 // Quantise Q, K and V, then attend.  With fuse_q, only K and V are quantised
 // here and the attention kernel quantises Q itself (q_dump / q_scale_dump
@@ -138,18 +211,10 @@ sage_status run_fused(const void* q, const void* k, const void* v, void* out, in
                                             at<float>(ws, w.kmean), st);
     if (e0 != cudaSuccess) return cuda_fail(e0, "K channel means launch");
   }
-  QKQuantArgs<__half> qa;
-  qa.q = static_cast<const uint16_t*>(q);
-  qa.k = static_cast<const uint16_t*>(k);
-  qa.q_codes = at<__half>(ws, w.q16);
-  qa.k_codes = at<__half>(ws, w.k16);
-  qa.q_scale = at<float>(ws, w.qs);
-  qa.k_scale = at<float>(ws, w.ks);
-  qa.BH = B * H;
-  qa.H = H;
-  qa.set_lengths(Sq, Sk);
-  qa.first = fuse_q ? 1 : 0;
-  qa.k_mean = smooth_k ? at<float>(ws, w.kmean) : nullptr;
+  const QKQuantArgs<__half> qa = staging_args(q, k, B, Sq, Sk, H, at<__half>(ws, w.q16), at<float>(ws, w.qs),
+                                              at<__half>(ws, w.k16), at<float>(ws, w.ks), fuse_q,
+                                              smooth_k ? at<float>(ws, w.kmean) : nullptr);
+  if (fault_fires(SAGE_FAULT_QUANT_LAUNCH)) return fail(SAGE_ERR_CUDA, "Q/K quantisation launch: injected fault");
   cudaError_t e = launch_qk_quantize<__half>(qa, st);
   if (e != cudaSuccess) return cuda_fail(e, "Q/K quantisation launch");
   e = launch_v_quantize(static_cast<const uint16_t*>(v), B, Sk, H, padded_len(Sk), at<uint32_t>(ws, w.vamax),
@@ -180,6 +245,7 @@ sage_status run_fused(const void* q, const void* k, const void* v, void* out, in
   aa.timeout_ns = timeout_ns();
   if (t_attn_before && (e = cudaEventRecord(t_attn_before, st)) != cudaSuccess)
     return cuda_fail(e, "timing event record");
+  if (fault_fires(SAGE_FAULT_ATTN_LAUNCH)) return fail(SAGE_ERR_CUDA, "attention launch: injected fault");
   e = launch_attention(aa, st);
   if (e != cudaSuccess) return cuda_fail(e, "attention launch");
   if (t_attn_after && (e = cudaEventRecord(t_attn_after, st)) != cudaSuccess)
@@ -285,8 +351,8 @@ sage_status sage_quantize_qkv(const void* q, const void* k, const void* v, int B
   cudaError_t e = launch_qk_quantize<int8_t>(qa, st);
   if (e != cudaSuccess) return cuda_fail(e, "Q/K quantisation launch");
   void* scratch = nullptr;
-  e = pool_alloc(&scratch, static_cast<size_t>(B) * H * kHeadDim * sizeof(uint32_t), st);
-  if (e != cudaSuccess) return fail(SAGE_ERR_NO_MEMORY, "scratch allocation failed: %s", cudaGetErrorString(e));
+  s = pool_alloc(&scratch, static_cast<size_t>(B) * H * kHeadDim * sizeof(uint32_t), st, "V maxima scratch");
+  if (s != SAGE_OK) return s;
   e = launch_v_quantize(static_cast<const uint16_t*>(v), B, S, H, Sp, static_cast<uint32_t*>(scratch), vt_fp8,
                         v_scale, st);
   cudaError_t e2 = cudaFreeAsync(scratch, st);
@@ -307,10 +373,10 @@ sage_status sage_quantize_qkv_smooth_k(const void* q, const void* k, const void*
   const size_t BH = static_cast<size_t>(B) * H;
   const size_t sum_bytes = align256(BH * kHeadDim * sizeof(unsigned long long));
   void* scratch = nullptr;
-  cudaError_t e = pool_alloc(&scratch, sum_bytes + BH * kHeadDim * sizeof(uint32_t), st);
-  if (e != cudaSuccess) return fail(SAGE_ERR_NO_MEMORY, "scratch allocation failed: %s", cudaGetErrorString(e));
+  s = pool_alloc(&scratch, sum_bytes + BH * kHeadDim * sizeof(uint32_t), st, "K sums and V maxima scratch");
+  if (s != SAGE_OK) return s;
   unsigned long long* sums = static_cast<unsigned long long*>(scratch);
-  e = launch_k_channel_means(static_cast<const uint16_t*>(k), B, S, H, sums, k_mean, st);
+  cudaError_t e = launch_k_channel_means(static_cast<const uint16_t*>(k), B, S, H, sums, k_mean, st);
   if (e == cudaSuccess) {
     QKQuantArgs<int8_t> qa;
     qa.q = static_cast<const uint16_t*>(q);
@@ -341,14 +407,9 @@ sage_status sage_attn_fwd_smooth_k(const void* q, const void* k, const void* v, 
   if (s == SAGE_OK) s = check_ptrs({{q, "q"}, {k, "k"}, {v, "v"}, {out, "out"}});
   if (s != SAGE_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  void* ws = nullptr;
-  cudaError_t e = pool_alloc(&ws, ws_layout(B, S, S, H).total, st);
-  if (e != cudaSuccess) return fail(SAGE_ERR_NO_MEMORY, "workspace allocation failed: %s", cudaGetErrorString(e));
-  s = run_fused(q, k, v, out, B, S, S, H, softmax_scale, ws, st, nullptr, false, nullptr, nullptr, true);
-  e = cudaFreeAsync(ws, st);
-  if (s != SAGE_OK) return s;
-  if (e != cudaSuccess) return cuda_fail(e, "workspace release");
-  return SAGE_OK;
+  return with_pool_workspace(ws_layout(B, S, S, H).total, st, [&](void* ws) {
+    return run_fused(q, k, v, out, B, S, S, H, softmax_scale, ws, st, nullptr, false, nullptr, nullptr, true);
+  });
 }
 
 sage_status sage_attn_fwd_ws(const void* q, const void* k, const void* v, void* out, int B, int S,
@@ -369,16 +430,9 @@ sage_status sage_attn_fwd(const void* q, const void* k, const void* v, void* out
   if (s == SAGE_OK) s = check_ptrs({{q, "q"}, {k, "k"}, {v, "v"}, {out, "out"}});
   if (s != SAGE_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  void* ws = nullptr;
-  cudaError_t e = pool_alloc(&ws, ws_layout(B, S, S, H).total, st);
-  if (e != cudaSuccess)
-    return fail(SAGE_ERR_NO_MEMORY, "workspace allocation of %zu bytes failed: %s", ws_layout(B, S, S, H).total,
-                cudaGetErrorString(e));
-  s = run_fused(q, k, v, out, B, S, S, H, softmax_scale, ws, st);
-  e = cudaFreeAsync(ws, st);
-  if (s != SAGE_OK) return s;
-  if (e != cudaSuccess) return cuda_fail(e, "workspace release");
-  return SAGE_OK;
+  return with_pool_workspace(ws_layout(B, S, S, H).total, st, [&](void* ws) {
+    return run_fused(q, k, v, out, B, S, S, H, softmax_scale, ws, st);
+  });
 }
 
 sage_status sage_attn_fwd_lse(const void* q, const void* k, const void* v, void* out, float* lse, int B,
@@ -388,16 +442,9 @@ sage_status sage_attn_fwd_lse(const void* q, const void* k, const void* v, void*
   if (s == SAGE_OK) s = check_ptrs({{q, "q"}, {k, "k"}, {v, "v"}, {out, "out"}, {lse, "lse"}});
   if (s != SAGE_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  void* ws = nullptr;
-  cudaError_t e = pool_alloc(&ws, ws_layout(B, S, S, H).total, st);
-  if (e != cudaSuccess)
-    return fail(SAGE_ERR_NO_MEMORY, "workspace allocation of %zu bytes failed: %s", ws_layout(B, S, S, H).total,
-                cudaGetErrorString(e));
-  s = run_fused(q, k, v, out, B, S, S, H, softmax_scale, ws, st, lse);
-  e = cudaFreeAsync(ws, st);
-  if (s != SAGE_OK) return s;
-  if (e != cudaSuccess) return cuda_fail(e, "workspace release");
-  return SAGE_OK;
+  return with_pool_workspace(ws_layout(B, S, S, H).total, st, [&](void* ws) {
+    return run_fused(q, k, v, out, B, S, S, H, softmax_scale, ws, st, lse);
+  });
 }
 
 sage_status sage_attn_fwd_cross(const void* q, const void* k, const void* v, void* out, float* lse, int B,
@@ -409,16 +456,9 @@ sage_status sage_attn_fwd_cross(const void* q, const void* k, const void* v, voi
   if (s == SAGE_OK && lse) s = check_ptrs({{lse, "lse"}});
   if (s != SAGE_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const size_t bytes = ws_layout(B, Sq, Skv, H).total;
-  void* ws = nullptr;
-  cudaError_t e = pool_alloc(&ws, bytes, st);
-  if (e != cudaSuccess)
-    return fail(SAGE_ERR_NO_MEMORY, "workspace allocation of %zu bytes failed: %s", bytes, cudaGetErrorString(e));
-  s = run_fused(q, k, v, out, B, Sq, Skv, H, softmax_scale, ws, st, lse);
-  e = cudaFreeAsync(ws, st);
-  if (s != SAGE_OK) return s;
-  if (e != cudaSuccess) return cuda_fail(e, "workspace release");
-  return SAGE_OK;
+  return with_pool_workspace(ws_layout(B, Sq, Skv, H).total, st, [&](void* ws) {
+    return run_fused(q, k, v, out, B, Sq, Skv, H, softmax_scale, ws, st, lse);
+  });
 }
 
 sage_status sage_attn_fwd_quantized(const int8_t* q_i8, const float* q_scale, const int8_t* k_i8,
@@ -460,14 +500,9 @@ sage_status sage_attn_fwd_fused_q(const void* q, const void* k, const void* v, v
   if (s == SAGE_OK) s = check_ptrs({{q, "q"}, {k, "k"}, {v, "v"}, {out, "out"}});
   if (s != SAGE_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  void* ws = nullptr;
-  cudaError_t e = pool_alloc(&ws, ws_layout(B, S, S, H).total, st);
-  if (e != cudaSuccess) return fail(SAGE_ERR_NO_MEMORY, "workspace allocation failed: %s", cudaGetErrorString(e));
-  s = run_fused(q, k, v, out, B, S, S, H, softmax_scale, ws, st, nullptr, true);
-  e = cudaFreeAsync(ws, st);
-  if (s != SAGE_OK) return s;
-  if (e != cudaSuccess) return cuda_fail(e, "workspace release");
-  return SAGE_OK;
+  return with_pool_workspace(ws_layout(B, S, S, H).total, st, [&](void* ws) {
+    return run_fused(q, k, v, out, B, S, S, H, softmax_scale, ws, st, nullptr, true);
+  });
 }
 
 sage_status sage_debug_fused_q(const void* q, const void* k, const void* v, void* out, int B, int S, int H,
@@ -478,13 +513,51 @@ sage_status sage_debug_fused_q(const void* q, const void* k, const void* v, void
     s = check_ptrs({{q, "q"}, {k, "k"}, {v, "v"}, {out, "out"}, {q_i8, "q_i8"}, {q_scale, "q_scale"}});
   if (s != SAGE_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  void* ws = nullptr;
-  cudaError_t e = pool_alloc(&ws, ws_layout(B, S, S, H).total, st);
-  if (e != cudaSuccess) return fail(SAGE_ERR_NO_MEMORY, "workspace allocation failed: %s", cudaGetErrorString(e));
-  s = run_fused(q, k, v, out, B, S, S, H, softmax_scale, ws, st, nullptr, true, q_i8, q_scale);
-  e = cudaFreeAsync(ws, st);
+  return with_pool_workspace(ws_layout(B, S, S, H).total, st, [&](void* ws) {
+    return run_fused(q, k, v, out, B, S, S, H, softmax_scale, ws, st, nullptr, true, q_i8, q_scale);
+  });
+}
+
+sage_status sage_debug_staging_codes(const void* q, const void* k, int B, int S, int H, int D, void* q16,
+                                     float* q_scale, void* k16, float* k_scale, void* stream) {
+  sage_status s = check_shape(B, S, H, D);
+  if (s == SAGE_OK)
+    s = check_ptrs({{q, "q"}, {k, "k"}, {q16, "q16"}, {q_scale, "q_scale"}, {k16, "k16"}, {k_scale, "k_scale"}});
   if (s != SAGE_OK) return s;
-  if (e != cudaSuccess) return cuda_fail(e, "workspace release");
+  const QKQuantArgs<__half> qa = staging_args(q, k, B, S, S, H, static_cast<__half*>(q16), q_scale,
+                                              static_cast<__half*>(k16), k_scale, false, nullptr);
+  cudaError_t e = launch_qk_quantize<__half>(qa, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "Q/K quantisation launch");
+  return SAGE_OK;
+}
+
+sage_status sage_debug_inject_fault(int site, int skip) {
+  if (site < SAGE_FAULT_NONE || site > SAGE_FAULT_ATTN_LAUNCH || skip < 0)
+    return fail(SAGE_ERR_INVALID_ARG, "fault site %d / skip %d out of range", site, skip);
+  g_fault_site.store(SAGE_FAULT_NONE, std::memory_order_relaxed);
+  g_fault_skip.store(skip, std::memory_order_relaxed);
+  g_fault_site.store(site, std::memory_order_relaxed);
+  return SAGE_OK;
+}
+
+sage_status sage_debug_pool_state(int* created, uint64_t* used_bytes) {
+  if (!created || !used_bytes) return fail(SAGE_ERR_INVALID_ARG, "created and used_bytes must not be NULL");
+  int dev = 0;
+  sage_status s = current_device(&dev);
+  if (s != SAGE_OK) return s;
+  cudaMemPool_t pool;
+  {
+    std::lock_guard<std::mutex> lk(g_pool_mu);
+    pool = g_pools[dev];
+  }
+  *created = pool != nullptr;
+  *used_bytes = 0;
+  if (pool) {
+    cuuint64_t used = 0;
+    cudaError_t e = cudaMemPoolGetAttribute(pool, cudaMemPoolAttrUsedMemCurrent, &used);
+    if (e != cudaSuccess) return cuda_fail(e, "memory pool query");
+    *used_bytes = static_cast<uint64_t>(used);
+  }
   return SAGE_OK;
 }
 

@@ -35,8 +35,12 @@ EXPORTED = (
     "sage_last_error", "sage_status_string", "sage_set_attention_events",
     "sage_quantize_qkv_noalloc", "sage_attn_fwd_lse", "sage_attn_fwd_cross",
     "sage_debug_fused_q", "sage_attn_fwd_fused_q", "sage_quantize_qkv_smooth_k",
-    "sage_attn_fwd_smooth_k", "sage_attn_fwd_launches",
+    "sage_attn_fwd_smooth_k", "sage_attn_fwd_launches", "sage_debug_staging_codes",
+    "sage_debug_inject_fault", "sage_debug_pool_state",
 )
+
+# Fault sites of sage_debug_inject_fault (include/sage.h).
+FAULT_NONE, FAULT_POOL_ALLOC, FAULT_QUANT_LAUNCH, FAULT_ATTN_LAUNCH = 0, 1, 2, 3
 
 
 class SageError(RuntimeError):
@@ -81,6 +85,9 @@ def load_library(path: str = LIB_PATH):
             "sage_attn_fwd_quantized": (S, [P, P, P, P, P, P, P, I, I, I, I, F, P, Z, P]),
             "sage_debug_qk_int32": (S, [P, P, P, P, P, P, P, P, I, I, I, I, F, P, Z, P]),
             "sage_debug_wait_timeout": (S, [ctypes.c_uint64, P]),
+            "sage_debug_staging_codes": (S, [P, P, I, I, I, I, P, P, P, P, P]),
+            "sage_debug_inject_fault": (S, [I, I]),
+            "sage_debug_pool_state": (S, [P, P]),
             "sage_sync_status": (S, [P]),
             "sage_set_wait_timeout_ns": (None, [ctypes.c_uint64]),
             "sage_set_attention_events": (None, [P, P]),
@@ -387,3 +394,36 @@ def set_attention_events(before=None, after=None):
         lib.sage_set_attention_events(None, None)
     else:
         lib.sage_set_attention_events(ctypes.c_void_p(before.cuda_event), ctypes.c_void_p(after.cuda_event))
+
+
+def debug_staging_codes(q, k):
+    """The Q/K quantisation exactly as sage_attn_fwd feeds the attention
+    kernel: (q16 fp16 [B,H,S_pad,D], q_scale [B,H,nb], k16, k_scale)."""
+    lib = load_library()
+    B, S, H, D = _check_qkv(q, k, k)
+    Sp = padded_len(S)
+    nb = (S + 31) // 32
+    dev = q.device
+    q16 = torch.empty((B, H, Sp, D), dtype=torch.float16, device=dev)
+    k16 = torch.empty_like(q16)
+    q_sc = torch.empty((B, H, nb), dtype=torch.float32, device=dev)
+    k_sc = torch.empty_like(q_sc)
+    with torch.cuda.device(dev):
+        _check(lib.sage_debug_staging_codes(_ptr(q), _ptr(k), B, S, H, D, _ptr(q16), _ptr(q_sc), _ptr(k16),
+                                            _ptr(k_sc), _stream(dev)))
+    return q16, q_sc, k16, k_sc
+
+
+def debug_inject_fault(site: int, skip: int = 0):
+    """Arm the library's host-side fault injection (FAULT_* sites)."""
+    _check(load_library().sage_debug_inject_fault(int(site), int(skip)))
+
+
+def debug_pool_state(device=None):
+    """(created, used_bytes) of the library's private memory pool on a device."""
+    lib = load_library()
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    created, used = ctypes.c_int(0), ctypes.c_uint64(0)
+    with torch.cuda.device(dev):
+        _check(lib.sage_debug_pool_state(ctypes.byref(created), ctypes.byref(used)))
+    return bool(created.value), int(used.value)

@@ -131,3 +131,18 @@ def test_binding_rejects_what_the_kernel_cannot_take():
     kb = torch.zeros((1, 4, 1, 128), dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         qad.attn_fwd(qb, kb, kb)      # cross-attention shape (shorter K/V)
+
+
+def test_test_hooks_check_their_arguments_on_the_host(lib):
+    assert lib.sage_debug_inject_fault(4, 0) == INVALID
+    assert lib.sage_debug_inject_fault(-1, 0) == INVALID
+    assert lib.sage_debug_inject_fault(1, -1) == INVALID
+    assert b"out of range" in lib.sage_last_error()
+    assert lib.sage_debug_inject_fault(0, 0) == OK          # disarm: no CUDA call
+    assert lib.sage_debug_pool_state(None, None) == INVALID
+    st = lib.sage_debug_staging_codes(P(FAKE), P(FAKE), 1, 64, 2, 64, *[P(FAKE)] * 4, None)
+    assert st == UNSUPPORTED
+    st = lib.sage_debug_staging_codes(P(FAKE), P(FAKE), 1, 64, 2, 128, P(FAKE), P(FAKE), P(FAKE + 8),
+                                      P(FAKE), None)
+    assert st == MISALIGNED
+    assert b"k16" in lib.sage_last_error()

@@ -9,6 +9,14 @@ InvokeAI PR #9657 "Summary" and diffusers PR #15060 "Results"):
   B=1 S=32760 H=40 (length not a multiple of the tile: tail blocks);
   B=1 S=65536 H=24 with per-channel K offsets (long video latent).
 The same launch configuration as the benchmark runs (sage_attn_fwd).
+
+Each sampled row is checked three ways: element-wise against the oracle's
+96-key online form, against its two-pass form within the derived bound of
+reading R16, and by cosine against unquantized float64 attention.  The
+cosine bar is 0.999 outright except on the outlier-channel workload, where
+the quantized algorithm itself (the oracle, tiled or two-pass) reaches only
+0.99891 on these rows: there the kernel must not fall more than 1e-4 below
+the oracle's own cosine.
 """
 import numpy as np
 import pytest
@@ -16,7 +24,8 @@ import torch
 
 import oracle
 from quantized_attention_diffusion_gb300.workloads import WORKLOADS, bf16_bits, make_workload, sample_rows
-from tests.gpu_common import COS_BAR, assert_close_to_oracle, cosine, ensure_library, f32
+from tests.gpu_common import (COS_BAR, assert_close_to_oracle, assert_within_two_pass_bound, cosine,
+                              ensure_library, f32)
 
 pytestmark = pytest.mark.gpu
 
@@ -26,6 +35,11 @@ def lib():
     if not torch.cuda.is_available():
         pytest.skip("needs a CUDA GPU")
     return ensure_library()
+
+
+# Workloads on which the quantized algorithm itself stays below the cosine
+# bar against float64 (measured with the oracle on the sampled rows).
+BELOW_BAR = {"b2_s16384_h24_outlier": 0.99891}
 
 
 @pytest.mark.parametrize("name", ["b2_s16384_h24_outlier", "b1_s32760_h40", "b1_s65536_h24_koffset"])
@@ -48,7 +62,12 @@ def test_full_size_sampled_rows(name):
     ref = f32(ref_bits)
     exact = oracle.attention_fp64(*bits, w.softmax_scale, rows=rows)
     err, n_ties = assert_close_to_oracle(got, ref, ties, name)
+    err2, used = assert_within_two_pass_bound(got, ref_quant, w.S, w.softmax_scale, rows, ties, name)
     cos_gpu, cos_oracle = cosine(got, exact), cosine(ref, exact)
-    print(f"{name}: max-abs vs oracle {err:.4g} ({n_ties} rows with P ties); cosine vs fp64 "
-          f"gpu {cos_gpu:.6f} oracle {cos_oracle:.6f}")
-    assert cos_gpu >= min(COS_BAR, cos_oracle - 1e-4)
+    print(f"{name}: max-abs vs oracle {err:.4g} ({n_ties} rows with P ties); vs two-pass {err2:.4g} "
+          f"({used:.3f} of the bound); cosine vs fp64 gpu {cos_gpu:.6f} oracle {cos_oracle:.6f}")
+    if name in BELOW_BAR:
+        assert cos_oracle < COS_BAR
+        assert cos_gpu >= cos_oracle - 1e-4
+    else:
+        assert cos_oracle >= COS_BAR and cos_gpu >= COS_BAR

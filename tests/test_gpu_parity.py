@@ -16,8 +16,9 @@ import pytest
 import torch
 
 import oracle
-from tests.gpu_common import (COS_BAR, assert_close_to_oracle, bf16_out_to_f32, cosine,
-                              default_scale, ensure_library, f32, gen, quant_to_dev)
+from tests.gpu_common import (COS_BAR, assert_close_to_oracle, assert_within_two_pass_bound,
+                              bf16_out_to_f32, cosine, default_scale, ensure_library, f32, gen,
+                              quant_to_dev)
 
 pytestmark = pytest.mark.gpu
 
@@ -102,6 +103,35 @@ def test_quantize_full_size_4096x24_bit_exact():
     _assert_quant_equal(_quantize_gpu(qkv), oracle.quantize(*bits))
 
 
+def _check_staging(qkv, bits):
+    """The fp16 codes sage_attn_fwd feeds the QK^T MMA equal the oracle's
+    INT8 codes as integers (fp16 holds every integer in [-127, 127] exactly;
+    a code 0 from a negative value may be -0, the same integer), and their
+    scales are bit-identical."""
+    import quantized_attention_diffusion_gb300 as qad
+    q16, qs, k16, ks = [t.cpu().numpy() for t in qad.debug_staging_codes(qkv[0].cuda(), qkv[1].cuda())]
+    for name, codes, scale, x in (("q", q16, qs, bits[0]), ("k", k16, ks, bits[1])):
+        ref_c, ref_s = oracle.quantize_qk(x)
+        vals = codes.astype(np.float64)
+        assert np.array_equal(vals, np.rint(vals)), name
+        eq = vals == ref_c.astype(np.float64)
+        if not eq.all():
+            bad = np.argwhere(~eq)[:5].tolist()
+            pytest.fail(f"{name}16: {int((~eq).sum())} codes differ, first at {bad}")
+        assert np.array_equal(scale.view(np.uint32), ref_s.view(np.uint32)), name
+
+
+@pytest.mark.parametrize("B,S,H,recipe,seed", SHAPES)
+def test_staging_codes_feeding_the_mma_equal_the_oracle(B, S, H, recipe, seed):
+    qkv, bits = gen(B, S, H, recipe, seed)
+    _check_staging(qkv, bits)
+
+
+def test_staging_codes_full_size_4096x24():
+    qkv, bits = gen(1, 4096, 24, "k_channel_offset", 1)
+    _check_staging(qkv, bits)
+
+
 # ---------------------------------------------------------- QK^T INT32 --
 
 @pytest.mark.parametrize("B,S,H,recipe,seed", [s for s in SHAPES if s[1] >= 31] +
@@ -121,19 +151,27 @@ def test_qk_int32_bit_exact(B, S, H, recipe, seed):
 
 # ------------------------------------------------------------- outputs --
 
-def _check_output(out_gpu, q_bits, k_bits, v_bits, scale, rows=None):
+def _check_output(out_gpu, q_bits, k_bits, v_bits, scale, rows=None, strict_cos=False):
+    """Element-wise against the oracle's 96-key online form (R7), against
+    its two-pass form within the bound of R16, and cosine against float64:
+    >= 0.999 outright with strict_cos (the pages' workloads of 256 and 4096
+    tokens, where the oracle itself clears it), else no more than 1e-4 below
+    the oracle's own (tiny or outlier-heavy shapes)."""
+    B, S, H, _ = q_bits.shape
     if rows is None:
-        ref_bits, ties = oracle.attention(q_bits, k_bits, v_bits, scale, return_ties=True)
-        exact = oracle.attention_fp64(q_bits, k_bits, v_bits, scale)
-        got = out_gpu
-    else:
-        ref_bits, ties = oracle.attention(q_bits, k_bits, v_bits, scale, rows=rows, return_ties=True)
-        exact = oracle.attention_fp64(q_bits, k_bits, v_bits, scale, rows=rows)
-        got = out_gpu[rows[:, 0], rows[:, 2], rows[:, 1]]
+        rows = oracle.all_rows(B, S, H)
+    quant = oracle.quantize(q_bits, k_bits, v_bits)
+    ref_bits, ties = oracle.attend_rows(quant, S, scale, rows, return_ties=True)
+    exact = oracle.attention_fp64(q_bits, k_bits, v_bits, scale, rows=rows)
+    got = out_gpu[rows[:, 0], rows[:, 2], rows[:, 1]]
     ref = f32(ref_bits)
     err, n_ties = assert_close_to_oracle(got, ref, ties, "output vs oracle")
+    assert_within_two_pass_bound(got, quant, S, scale, rows, ties, "output vs two-pass oracle")
     cos_gpu, cos_oracle = cosine(got, exact), cosine(ref, exact)
-    assert cos_gpu >= min(COS_BAR, cos_oracle - 1e-4), (cos_gpu, cos_oracle)
+    if strict_cos:
+        assert cos_oracle >= COS_BAR and cos_gpu >= COS_BAR, (cos_gpu, cos_oracle)
+    else:
+        assert cos_gpu >= min(COS_BAR, cos_oracle - 1e-4), (cos_gpu, cos_oracle)
     return err, cos_gpu, cos_oracle
 
 
@@ -142,14 +180,15 @@ def test_attention_matches_oracle(B, S, H, recipe, seed):
     import quantized_attention_diffusion_gb300 as qad
     qkv, bits = gen(B, S, H, recipe, seed)
     out = qad.attn_fwd(*[t.cuda() for t in qkv], softmax_scale=default_scale())
-    _check_output(bf16_out_to_f32(out), *bits, default_scale())
+    _check_output(bf16_out_to_f32(out), *bits, default_scale(),
+                  strict_cos=(B, S, H, recipe, seed) == (1, 256, 2, "normal", 0))
 
 
 def test_attention_full_size_4096x24_matches_oracle():
     import quantized_attention_diffusion_gb300 as qad
     qkv, bits = gen(1, 4096, 24, "k_channel_offset", 1)
     out = qad.attn_fwd(*[t.cuda() for t in qkv])
-    _check_output(bf16_out_to_f32(out), *bits, default_scale())
+    _check_output(bf16_out_to_f32(out), *bits, default_scale(), strict_cos=True)
 
 
 def test_fused_path_equals_quantize_then_attend():
