@@ -9,9 +9,10 @@ attention throughput, TOPS = 4*B*H*S^2*D / step time.
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
                   [--impl ours|reference]
 
-N > 1 runs N independent replicas (one process per GPU under torchrun; the
-method has no exchange step on one call), reports the whole-job throughput
-and takes the maximum time over ranks.  ``--impl reference`` times the CPU
+N > 1 runs N independent replicas, one process per GPU (the method has no
+exchange step in one call): under torchrun each rank is one replica; run
+directly, bench.py starts the N rank processes itself.  The line reports the
+whole-job throughput over the maximum time of the ranks.  ``--impl reference`` times the CPU
 oracle (the only stand-in for a reference implementation: none exists for
 this hardware) on a bounded sample of the same workload.
 """
@@ -59,6 +60,8 @@ def parse_args():
                     help="time sage_attn_fwd_smooth_k (K loses its per-channel mean before quantisation)")
     ap.add_argument("--no-e2e", action="store_true",
                     help="skip the host-buffer leg (for short profiling runs; the line then has no e2e figure)")
+    ap.add_argument("--launcher-selftest", action="store_true",
+                    help="CPU check of the replica launcher and rank plumbing (gloo): no GPU, no metric")
     return ap.parse_args()
 
 
@@ -101,6 +104,28 @@ class Group:
             self.dist.destroy_process_group()
 
 
+def free_port() -> int:
+    import socket
+    with socket.socket() as sock:
+        sock.bind(("127.0.0.1", 0))
+        return sock.getsockname()[1]
+
+
+def launch_replicas(n: int, argv) -> int:
+    """Run this script as n rank processes (RANK = LOCAL_RANK = 0..n-1,
+    WORLD_SIZE = n, rendezvous on 127.0.0.1), one GPU each; rank 0's output
+    passes through.  Returns the worst exit code."""
+    port = str(free_port())
+    procs = []
+    for r in range(n):
+        env = dict(os.environ, RANK=str(r), LOCAL_RANK=str(r), WORLD_SIZE=str(n),
+                   LOCAL_WORLD_SIZE=str(n), MASTER_ADDR="127.0.0.1", MASTER_PORT=port)
+        out = None if r == 0 else subprocess.DEVNULL
+        procs.append(subprocess.Popen([sys.executable, os.path.abspath(__file__), *argv], env=env, stdout=out))
+    codes = [p.wait() for p in procs]
+    return max(codes, key=abs)
+
+
 def job_tops(world: int, ops_per_call: float, calls_per_rank: int, ms_max: float) -> float:
     """Whole-job throughput of weak-scaled replicas: every rank runs the
     same number of calls; the slowest rank's time bounds the job."""
@@ -110,81 +135,146 @@ def job_tops(world: int, ops_per_call: float, calls_per_rank: int, ms_max: float
 # --------------------------------------------------------------- clocks --
 
 class ClockSampler:
-    """nvidia-smi samples (every 200 ms) of the SM clock and throttle reasons."""
+    """SM clock, power and clock-event reasons of one GPU, read through NVML
+    (read-only queries) every `period_s` by a background thread; `stop`
+    keeps the samples taken inside [t0, t1], the host times that bracket
+    the timed region.  Falls back to `nvidia-smi -lms 20` without NVML."""
 
-    FIELDS = ["clocks.sm", "clocks.max.sm", "clocks_event_reasons.hw_slowdown",
-              "clocks_event_reasons.hw_thermal_slowdown", "clocks_event_reasons.sw_thermal_slowdown",
-              "clocks_event_reasons.sw_power_cap", "power.draw"]
+    # nvmlClocksEventReasons bits
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
 
-    def __init__(self, gpu_index: int):
-        self.gpu = gpu_index
-        self.proc = None
-        self.file = None
+    def __init__(self, cuda_index: int, period_s: float = 0.005):
+        self.cuda_index, self.period = cuda_index, period_s
+        self.samples, self.source = [], None
+        self.thread = self.proc = None
+        self.stop_flag = False
+
+    def _nvml_handle(self):
+        import ctypes
+        nvml = ctypes.CDLL("libnvidia-ml.so.1")
+        if nvml.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        h = ctypes.c_void_p()
+        uuid = None
+        try:
+            import torch
+            uuid = str(torch.cuda.get_device_properties(self.cuda_index).uuid)
+        except Exception:
+            pass
+        ok = -1
+        if uuid:
+            uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+            ok = nvml.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(h))
+        if ok != 0:
+            ok = nvml.nvmlDeviceGetHandleByIndex_v2(self.cuda_index, ctypes.byref(h))
+        if ok != 0:
+            raise OSError("no NVML handle")
+        return nvml, h
 
     def start(self):
+        import threading
+        try:
+            nvml, h = self._nvml_handle()
+        except OSError:
+            return self._start_smi()
+        import ctypes
+        reasons_fn = getattr(nvml, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            nvml.nvmlDeviceGetCurrentClocksThrottleReasons
+        mx = ctypes.c_uint(0)
+        nvml.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx))
+        self.max_mhz = float(mx.value)
+        self.source = "nvml"
+
+        def run():
+            sm, pw, rs = ctypes.c_uint(0), ctypes.c_uint(0), ctypes.c_ulonglong(0)
+            while not self.stop_flag:
+                t = time.perf_counter()
+                if nvml.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(sm)) == 0:
+                    nvml.nvmlDeviceGetPowerUsage(h, ctypes.byref(pw))
+                    reasons_fn(h, ctypes.byref(rs))
+                    self.samples.append((t, float(sm.value), pw.value / 1000.0, int(rs.value)))
+                time.sleep(self.period)
+
+        self.thread = threading.Thread(target=run, daemon=True)
+        self.thread.start()
+
+    def _start_smi(self):
+        fields = "clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active"
         try:
             self.file = tempfile.TemporaryFile(mode="w+")
+            self.t_smi0 = time.perf_counter()
             self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={','.join(self.FIELDS)}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
-                stdout=self.file, stderr=subprocess.DEVNULL)
+                ["nvidia-smi", "-i", str(self.cuda_index), f"--query-gpu={fields}",
+                 "--format=csv,noheader,nounits", "-lms", "20"], stdout=self.file, stderr=subprocess.DEVNULL)
+            self.source = "nvidia-smi"
         except OSError:
             self.proc = None
 
-    def stop(self):
-        if not self.proc:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.proc.kill()
-        self.file.seek(0)
-        sm, smax, reasons, power = [], [], set(), []
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in self.file.read().splitlines():
-            f = [x.strip() for x in line.split(",")]
-            if len(f) != len(self.FIELDS):
-                continue
+    def stop(self, t0: float, t1: float):
+        if self.thread is not None:
+            self.stop_flag = True
+            self.thread.join(timeout=5)
+            rows = [(sm, pw, rs) for t, sm, pw, rs in self.samples if t0 <= t <= t1]
+            smax = self.max_mhz
+        elif self.proc is not None:
+            self.proc.terminate()
             try:
-                sm.append(float(f[0]))
-                smax.append(float(f[1]))
-                power.append(float(f[6]))
-            except ValueError:
-                continue
-            for n, val in zip(names, f[2:6]):
-                if val.lower() == "active":
-                    reasons.add(n)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
-                "samples": len(sm), "power_w_max": max(power) if power else None}
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.file.seek(0)
+            rows, smax = [], None
+            for line in self.file.read().splitlines():
+                f = [x.strip() for x in line.split(",")]
+                try:
+                    rows.append((float(f[0]), float(f[2]), int(f[3], 16)))
+                    smax = float(f[1])
+                except (ValueError, IndexError):
+                    continue
+        else:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no clock source"]}
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": smax, "reasons": ["no samples"], "source": self.source}
+        reasons = sorted({name for _, _, rs in rows for bit, name in self.REASONS.items() if rs & bit})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": smax, "reasons": reasons,
+                "samples": len(rows), "sm_mhz_min": min(r[0] for r in rows),
+                "power_w_max": max(r[1] for r in rows), "source": self.source,
+                "period_ms": round(self.period * 1e3, 1) if self.source == "nvml" else 20}
 
 
 # ---------------------------------------------------------------- peaks --
 
 def tensor_peak():
-    """Dense peak of the attention kernel's mixed contraction (TFLOP/s).
+    """Dense peaks of the attention kernel's mixed contraction (TFLOP/s).
 
-    QK^T runs at the fp16/bf16 tensor rate (the measured cuBLAS bf16 figure),
-    PV at the E4M3 rate (2x, the nominal fp8/bf16 ratio).  Half the ops run
-    at each rate, so the combined peak is 4 / (2/P + 2/(2P)) = 4P/3.  The
-    sustained figure is the headline denominator (the kernel runs back to
-    back for the whole timed region); the burst figure is returned too.
-    """
+    QK^T runs at the fp16/bf16 tensor rate P (the measured cuBLAS bf16
+    figure), PV on E4M3 at 2P (the ratio our tcgen05 probe measured per MMA:
+    M=128, N=256, kind::f16 with K=16 and kind::f8f6f4 with K=32 both take
+    128 SM clocks).  Half the ops run at each rate, so the combined peak is
+    4 / (2/P + 2/(2P)) = 4P/3.  The headline uses the burst P (a kernel timed
+    on its own, at the clock it ran at); the sustained P (a seconds-long,
+    power-capped GEMM loop) is returned too.
+    Returns (burst, sustained, bf16 burst, hbm GB/s, source)."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     src = "fallback"
-    p_bf16, p_burst, hbm = 1700.0, 1900.0, 6800.0
+    p_burst, p_sust, hbm = 1900.0, 1700.0, 6800.0
     try:
         with open(path) as f:
             m = json.load(f)
-        p_bf16 = float(m["bf16_tflops_sustained"])
-        p_burst = float(m.get("bf16_tflops", p_bf16))
+        p_burst = float(m["bf16_tflops"])
+        p_sust = float(m.get("bf16_tflops_sustained", p_burst))
         hbm = float(m["hbm_gbs"])
         src = "measured"
     except (OSError, KeyError, ValueError):
         pass
-    return 4.0 * p_bf16 / 3.0, p_bf16, hbm, src, 4.0 * p_burst / 3.0
+    return 4.0 * p_burst / 3.0, 4.0 * p_sust / 3.0, p_burst, hbm, src
+
+
+# tcgen05 dense rate per SM and clock at M=128: 8192 fp16 flop (our probe:
+# N=256, K=16 in 128 clocks), E4M3 twice that; GB300 has 152 SMs.
+FP16_FLOP_PER_CLK_SM = 8192
+N_SMS = 152
 
 
 def attention_traffic():
@@ -282,16 +372,18 @@ def run_ours(args, group, local):
     group.barrier()
     torch.cuda.synchronize()
     sampler.start()
-    time.sleep(0.3)
+    time.sleep(0.1)
+    t0 = time.perf_counter()
     start.record()
     for i in range(K):
         qad.set_attention_events(before[i], after[i])
         step(q, k, v, out, lse)
     end.record()
     torch.cuda.synchronize()
+    t1 = time.perf_counter()
     qad.set_attention_events()
     group.barrier()
-    clocks = sampler.stop()
+    clocks = sampler.stop(t0, t1)
     ms = start.elapsed_time(end)
     attn_ms = statistics.mean(b.elapsed_time(a) for b, a in zip(before, after))
     ms_max = group.max(ms)
@@ -359,8 +451,11 @@ def run_ours(args, group, local):
     in_bytes = (q.numel() + k.numel() + v.numel()) * q.element_size()
     out_bytes = out.numel() * out.element_size() + (lse.numel() * 4 if args.lse else 0)
 
-    peak, p_bf16, hbm, src, peak_burst = tensor_peak()
+    peak, peak_sust, p_bf16, hbm, src = tensor_peak()
     achieved = w.ops / (attn_ms_max * 1e-3) / 1e12
+    clock_peak = None
+    if clocks.get("sm_mhz"):
+        clock_peak = 4.0 / 3.0 * FP16_FLOP_PER_CLK_SM * N_SMS * clocks["sm_mhz"] * 1e6 / 1e12
     line = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -393,8 +488,11 @@ def run_ours(args, group, local):
             "bound": "tensor", "achieved": round(achieved, 1), "peak": round(peak, 1), "unit": "TFLOP/s",
             "frac": round(achieved / peak, 4), "traffic": attention_traffic(),
             "kernel": "sage_attn_kernel", "attention_ms_per_launch": round(attn_ms_max, 4),
-            "peak_basis": f"{src} bf16 sustained {p_bf16} TFLOP/s for QK^T (fp16 rate), x2 for E4M3 PV",
-            "peak_burst": round(peak_burst, 1), "frac_vs_burst": round(achieved / peak_burst, 4),
+            "peak_basis": f"{src} cuBLAS bf16 burst {p_bf16} TFLOP/s (of measured) for QK^T at the fp16 rate, "
+                          f"2x for E4M3 PV (per-MMA ratio measured by a tcgen05 probe): 4P/3",
+            "peak_sustained": round(peak_sust, 1), "frac_vs_sustained": round(achieved / peak_sust, 4),
+            "peak_at_sampled_clock": round(clock_peak, 1) if clock_peak else None,
+            "frac_vs_sampled_clock": round(achieved / clock_peak, 4) if clock_peak else None,
         },
         "clocks": clocks,
     }
@@ -433,9 +531,27 @@ def run_reference(args):
     }
 
 
+def launcher_selftest(world, rank, local):
+    """Rank plumbing on CPU (gloo): barrier, then the max of per-rank times;
+    rank 0 prints what the real line's n_gpus and ms_max would be."""
+    group = Group(world, rank, local, use_cuda=False)
+    try:
+        group.barrier()
+        ms_max = group.max(10.0 + rank)
+        group.barrier()
+        if rank == 0:
+            print(json.dumps({"launcher_selftest": True, "n_gpus": group.world, "ms_max": ms_max}), flush=True)
+    finally:
+        group.close()
+
+
 def main():
     args = parse_args()
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ and args.impl == "ours":
+        sys.exit(launch_replicas(args.gpus, sys.argv[1:]))
     world, rank, local = dist_env()
+    if args.launcher_selftest:
+        return launcher_selftest(world, rank, local)
     if args.impl == "reference":
         if rank == 0:
             print(json.dumps(run_reference(args)), flush=True)

@@ -57,3 +57,19 @@ def test_single_process_group_is_a_no_op():
     g.barrier()
     assert g.max(3.25) == 3.25
     g.close()
+
+
+def test_bench_gpus_2_starts_two_ranks_itself():
+    """`bench.py --gpus 2`, run directly (no torchrun), starts its own two
+    rank processes; in the CPU self-test mode they meet over gloo and rank 0
+    prints n_gpus = 2 and the maximum over the ranks' times."""
+    import json
+    import subprocess
+    env = {k: v for k, v in os.environ.items() if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK")}
+    res = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--gpus", "2", "--launcher-selftest"],
+                         capture_output=True, text=True, timeout=300, env=env, cwd=ROOT)
+    assert res.returncode == 0, res.stderr[-2000:]
+    lines = [ln for ln in res.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, res.stdout
+    rec = json.loads(lines[0])
+    assert rec["n_gpus"] == 2 and rec["ms_max"] == 11.0
