@@ -112,11 +112,10 @@ struct CodeStore<__half> {
 // odd ones, lane%16 owns channels 8*(lane%16) .. +7: a load or store
 // instruction of the warp covers two whole 256-byte token rows.  A lane loads
 // all its 16 tokens before anything else (256 bytes in flight), and the block
-// max is a warp shuffle: no shared memory, no block-wide barrier.  grid.y
+// max is a warp shuffle: no shared memory, no block-wide barrier.  `tensor`
 // selects Q (0) or K (1).
 template <typename CodeT, bool kSmooth>
-__global__ void __launch_bounds__(256, 2) qk_quantize_kernel(QKQuantArgs<CodeT> a) {
-  const int tensor = blockIdx.y + a.first;
+__device__ __forceinline__ void qk_warp(const QKQuantArgs<CodeT>& a, int tensor) {
   const uint16_t* __restrict__ x = tensor == 0 ? a.q : a.k;
   CodeT* __restrict__ codes = tensor == 0 ? a.q_codes : a.k_codes;
   float* __restrict__ scale = tensor == 0 ? a.q_scale : a.k_scale;
@@ -189,18 +188,19 @@ __global__ void __launch_bounds__(256, 2) qk_quantize_kernel(QKQuantArgs<CodeT> 
   }
 }
 
-// Per-channel |v| maxima.  grid = (ceil(S / kVRowsPerCta), B*H), 256 threads;
-// thread t owns channels 8*(t%16) .. +7 of every 16th token.  Results are
-// merged with atomicMax on the fp32 bit patterns (order-preserving for
-// non-negative values) into amax_bits [B*H, 128], which must start at 0.
+// Per-channel |v| maxima of one 256-token slice of one (batch, head), by a
+// whole CTA of 256 threads: thread t owns channels 8*(t%16) .. +7 of every
+// 16th token.  Results are merged with atomicMax on the fp32 bit patterns
+// (order-preserving for non-negative values) into amax_bits [B*H, 128], which
+// must start at 0.
 constexpr int kVRowsPerCta = 256;
 
-__global__ void __launch_bounds__(256) v_amax_kernel(const uint16_t* __restrict__ v, int S, int H,
-                                                     uint32_t* __restrict__ amax_bits) {
+__device__ __forceinline__ void v_amax_slice(const uint16_t* __restrict__ v, int S, int H,
+                                             uint32_t* __restrict__ amax_bits, int bh, int slice) {
   __shared__ float part[16][kHeadDim];
-  const int bh = blockIdx.y, b = bh / H, h = bh % H;
+  const int b = bh / H, h = bh % H;
   const int t = threadIdx.x, c8 = (t & 15) * 8, r = t >> 4;
-  const int s0 = blockIdx.x * kVRowsPerCta;
+  const int s0 = slice * kVRowsPerCta;
   const int s1 = min(S, s0 + kVRowsPerCta);
   const size_t tok_stride = static_cast<size_t>(H) * kHeadDim;
   const uint16_t* src = v + (static_cast<size_t>(b) * S * H + h) * kHeadDim + c8;
@@ -223,6 +223,28 @@ __global__ void __launch_bounds__(256) v_amax_kernel(const uint16_t* __restrict_
     for (int i = 1; i < 16; ++i) mm = fmaxf(mm, part[i][t]);
     atomicMax(amax_bits + static_cast<size_t>(bh) * kHeadDim + t, __float_as_uint(mm));
   }
+}
+
+// First quantisation pass, one launch: Q and K codes (grid.y role 0 and 1,
+// qk_warp) and the per-channel V maxima (role 2, one CTA per 256-token slice
+// of one (batch, head)).  The roles are CTA-uniform.
+struct VMaxArgs {
+  const uint16_t* v;      // bf16 [B, S, H, 128]; nullptr: no V maxima
+  uint32_t* amax_bits;    // [B*H, 128], zeroed before the launch
+  int S, H, BH, nslices;  // nslices = ceil(S / kVRowsPerCta)
+};
+
+template <typename CodeT, bool kSmooth>
+__global__ void __launch_bounds__(256, 2) qkv_pass1_kernel(QKQuantArgs<CodeT> a, VMaxArgs vm) {
+  const int role = blockIdx.y + a.first;
+  if (role == 2) {
+    const long long idx = blockIdx.x;
+    if (idx >= static_cast<long long>(vm.BH) * vm.nslices) return;   // CTA-uniform
+    v_amax_slice(vm.v, vm.S, vm.H, vm.amax_bits, static_cast<int>(idx / vm.nslices),
+                 static_cast<int>(idx % vm.nslices));
+    return;
+  }
+  qk_warp<CodeT, kSmooth>(a, role);
 }
 
 // A bf16 value times 2^40 as a 64-bit integer: exact for |x| in [2^-33, 2^22)
@@ -387,30 +409,37 @@ __global__ void __launch_bounds__(256) widen_codes_kernel(const int8_t* __restri
 }  // namespace
 
 template <typename CodeT>
-cudaError_t launch_qk_quantize(const QKQuantArgs<CodeT>& a, cudaStream_t stream) {
+cudaError_t launch_qkv_quantize(const QKQuantArgs<CodeT>& a, const uint16_t* v, uint32_t* amax_bits, uint8_t* vt,
+                                float* v_scale, cudaStream_t stream) {
+  VMaxArgs vm;
+  vm.v = v;
+  vm.amax_bits = amax_bits;
+  vm.S = a.S[1];
+  vm.H = a.H;
+  vm.BH = a.BH;
+  vm.nslices = (a.S[1] + kVRowsPerCta - 1) / kVRowsPerCta;
+  if (v != nullptr) {
+    cudaError_t e = cudaMemsetAsync(amax_bits, 0, static_cast<size_t>(a.BH) * kHeadDim * sizeof(uint32_t), stream);
+    if (e != cudaSuccess) return e;
+  }
   const long long blocks = static_cast<long long>(a.BH) * (std::max(a.first ? 0 : a.S_pad[0], a.S_pad[1]) / 32);
-  const long long ctas = (blocks + 7) / 8;
-  const dim3 grid(static_cast<unsigned>(ctas), 2 - a.first);
+  long long ctas = (blocks + 7) / 8;
+  if (v != nullptr) ctas = std::max(ctas, static_cast<long long>(a.BH) * vm.nslices);
+  const dim3 grid(static_cast<unsigned>(ctas), (v != nullptr ? 3 : 2) - a.first);
   if (a.k_mean != nullptr)
-    qk_quantize_kernel<CodeT, true><<<grid, 256, 0, stream>>>(a);
+    qkv_pass1_kernel<CodeT, true><<<grid, 256, 0, stream>>>(a, vm);
   else
-    qk_quantize_kernel<CodeT, false><<<grid, 256, 0, stream>>>(a);
+    qkv_pass1_kernel<CodeT, false><<<grid, 256, 0, stream>>>(a, vm);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || v == nullptr) return e;
+  const int S_pad = a.S_pad[1];
+  v_encode_kernel<<<dim3(S_pad / 128, a.BH), 256, 0, stream>>>(v, a.S[1], a.H, S_pad, amax_bits, vt, v_scale);
   return cudaGetLastError();
 }
-template cudaError_t launch_qk_quantize<int8_t>(const QKQuantArgs<int8_t>&, cudaStream_t);
-template cudaError_t launch_qk_quantize<__half>(const QKQuantArgs<__half>&, cudaStream_t);
-
-cudaError_t launch_v_quantize(const uint16_t* v, int B, int S, int H, int S_pad, uint32_t* amax_bits,
-                              uint8_t* vt, float* v_scale, cudaStream_t stream) {
-  const int BH = B * H;
-  cudaError_t e = cudaMemsetAsync(amax_bits, 0, static_cast<size_t>(BH) * kHeadDim * sizeof(uint32_t), stream);
-  if (e != cudaSuccess) return e;
-  v_amax_kernel<<<dim3((S + kVRowsPerCta - 1) / kVRowsPerCta, BH), 256, 0, stream>>>(v, S, H, amax_bits);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  v_encode_kernel<<<dim3(S_pad / 128, BH), 256, 0, stream>>>(v, S, H, S_pad, amax_bits, vt, v_scale);
-  return cudaGetLastError();
-}
+template cudaError_t launch_qkv_quantize<int8_t>(const QKQuantArgs<int8_t>&, const uint16_t*, uint32_t*, uint8_t*,
+                                                 float*, cudaStream_t);
+template cudaError_t launch_qkv_quantize<__half>(const QKQuantArgs<__half>&, const uint16_t*, uint32_t*, uint8_t*,
+                                                 float*, cudaStream_t);
 
 cudaError_t launch_k_channel_means(const uint16_t* k, int B, int S, int H, unsigned long long* sums, float* mean,
                                    cudaStream_t stream) {

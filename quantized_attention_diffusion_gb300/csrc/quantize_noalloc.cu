@@ -96,7 +96,6 @@ extern "C" sage_status sage_quantize_qkv_noalloc(const void* q, const void* k, c
   uint32_t* scratch = scratch_for_current_device();
   if (!scratch) return SAGE_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const int Sp = sage::padded_len(S);
   sage::QKQuantArgs<int8_t> qa;
   qa.q = static_cast<const uint16_t*>(q);
   qa.k = static_cast<const uint16_t*>(k);
@@ -107,11 +106,9 @@ extern "C" sage_status sage_quantize_qkv_noalloc(const void* q, const void* k, c
   qa.BH = B * H;
   qa.H = H;
   qa.set_lengths(S, S);
-  cudaError_t e = sage::launch_qk_quantize<int8_t>(qa, st);
-  // launch_v_quantize zeroes the maxima (cudaMemsetAsync, no allocation)
+  // launch_qkv_quantize zeroes the maxima (cudaMemsetAsync, no allocation)
   // before reducing into them, so the previous call's contents never leak.
-  if (e == cudaSuccess)
-    e = sage::launch_v_quantize(static_cast<const uint16_t*>(v), B, S, H, Sp, scratch, vt_fp8, v_scale, st);
+  cudaError_t e = sage::launch_qkv_quantize<int8_t>(qa, static_cast<const uint16_t*>(v), scratch, vt_fp8, v_scale, st);
   if (e != cudaSuccess) {
     sage::set_last_error("quantisation launch failed: %s", cudaGetErrorString(e));
     return SAGE_ERR_CUDA;

@@ -198,6 +198,24 @@ QKQuantArgs<__half> staging_args(const void* q, const void* k, int B, int Sq, in
   return qa;
 }
 
+// Arguments of the public INT8 quantisation (sage_quantize_qkv and its
+// variants): codes [B, H, S_pad, 128].
+QKQuantArgs<int8_t> public_args(const void* q, const void* k, int B, int S, int H, int8_t* q_i8, float* q_scale,
+                                int8_t* k_i8, float* k_scale, const float* k_mean) {
+  QKQuantArgs<int8_t> qa;
+  qa.q = static_cast<const uint16_t*>(q);
+  qa.k = static_cast<const uint16_t*>(k);
+  qa.q_codes = q_i8;
+  qa.k_codes = k_i8;
+  qa.q_scale = q_scale;
+  qa.k_scale = k_scale;
+  qa.BH = B * H;
+  qa.H = H;
+  qa.set_lengths(S, S);
+  qa.k_mean = k_mean;
+  return qa;
+}
+
 // Quantise Q, K and V, then attend.  With fuse_q, only K and V are quantised
 // here and the attention kernel quantises Q itself (q_dump / q_scale_dump
 // then receive its codes and scales, if given).
@@ -214,12 +232,10 @@ sage_status run_fused(const void* q, const void* k, const void* v, void* out, in
   const QKQuantArgs<__half> qa = staging_args(q, k, B, Sq, Sk, H, at<__half>(ws, w.q16), at<float>(ws, w.qs),
                                               at<__half>(ws, w.k16), at<float>(ws, w.ks), fuse_q,
                                               smooth_k ? at<float>(ws, w.kmean) : nullptr);
-  if (fault_fires(SAGE_FAULT_QUANT_LAUNCH)) return fail(SAGE_ERR_CUDA, "Q/K quantisation launch: injected fault");
-  cudaError_t e = launch_qk_quantize<__half>(qa, st);
-  if (e != cudaSuccess) return cuda_fail(e, "Q/K quantisation launch");
-  e = launch_v_quantize(static_cast<const uint16_t*>(v), B, Sk, H, padded_len(Sk), at<uint32_t>(ws, w.vamax),
-                        at<uint8_t>(ws, w.vt), at<float>(ws, w.vs), st);
-  if (e != cudaSuccess) return cuda_fail(e, "V quantisation launch");
+  if (fault_fires(SAGE_FAULT_QUANT_LAUNCH)) return fail(SAGE_ERR_CUDA, "quantisation launch: injected fault");
+  cudaError_t e = launch_qkv_quantize<__half>(qa, static_cast<const uint16_t*>(v), at<uint32_t>(ws, w.vamax),
+                                              at<uint8_t>(ws, w.vt), at<float>(ws, w.vs), st);
+  if (e != cudaSuccess) return cuda_fail(e, "quantisation launch");
   AttnArgs aa;
   aa.q_bf16 = fuse_q ? static_cast<const uint16_t*>(q) : nullptr;
   aa.q_dump = q_dump;
@@ -317,9 +333,9 @@ int64_t sage_padded_len(int S) { return S < 1 ? 0 : static_cast<int64_t>(padded_
 
 int sage_attn_fwd_launches(int B, int Sq, int Skv, int H, int smooth_k) {
   if (B < 1 || Sq < 1 || Skv < 1 || H < 1) return -1;
-  // Q/K quantisation, V maxima, V encoding, attention; K smoothing adds the
-  // channel sums and means.
-  return 4 + (smooth_k ? 2 : 0);
+  // Q/K quantisation with the V maxima, V encoding, attention; K smoothing
+  // adds the channel sums and means.
+  return 3 + (smooth_k ? 2 : 0);
 }
 
 size_t sage_workspace_bytes(int B, int S, int H, int D) {
@@ -337,26 +353,14 @@ sage_status sage_quantize_qkv(const void* q, const void* k, const void* v, int B
                     {k_scale, "k_scale"}, {vt_fp8, "vt_fp8"}, {v_scale, "v_scale"}});
   if (s != SAGE_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const int Sp = padded_len(S);
-  QKQuantArgs<int8_t> qa;
-  qa.q = static_cast<const uint16_t*>(q);
-  qa.k = static_cast<const uint16_t*>(k);
-  qa.q_codes = q_i8;
-  qa.k_codes = k_i8;
-  qa.q_scale = q_scale;
-  qa.k_scale = k_scale;
-  qa.BH = B * H;
-  qa.H = H;
-  qa.set_lengths(S, S);
-  cudaError_t e = launch_qk_quantize<int8_t>(qa, st);
-  if (e != cudaSuccess) return cuda_fail(e, "Q/K quantisation launch");
   void* scratch = nullptr;
   s = pool_alloc(&scratch, static_cast<size_t>(B) * H * kHeadDim * sizeof(uint32_t), st, "V maxima scratch");
   if (s != SAGE_OK) return s;
-  e = launch_v_quantize(static_cast<const uint16_t*>(v), B, S, H, Sp, static_cast<uint32_t*>(scratch), vt_fp8,
-                        v_scale, st);
+  const QKQuantArgs<int8_t> qa = public_args(q, k, B, S, H, q_i8, q_scale, k_i8, k_scale, nullptr);
+  cudaError_t e = launch_qkv_quantize<int8_t>(qa, static_cast<const uint16_t*>(v), static_cast<uint32_t*>(scratch),
+                                              vt_fp8, v_scale, st);
   cudaError_t e2 = cudaFreeAsync(scratch, st);
-  if (e != cudaSuccess) return cuda_fail(e, "V quantisation launch");
+  if (e != cudaSuccess) return cuda_fail(e, "quantisation launch");
   if (e2 != cudaSuccess) return cuda_fail(e2, "scratch release");
   return SAGE_OK;
 }
@@ -378,22 +382,10 @@ sage_status sage_quantize_qkv_smooth_k(const void* q, const void* k, const void*
   unsigned long long* sums = static_cast<unsigned long long*>(scratch);
   cudaError_t e = launch_k_channel_means(static_cast<const uint16_t*>(k), B, S, H, sums, k_mean, st);
   if (e == cudaSuccess) {
-    QKQuantArgs<int8_t> qa;
-    qa.q = static_cast<const uint16_t*>(q);
-    qa.k = static_cast<const uint16_t*>(k);
-    qa.q_codes = q_i8;
-    qa.k_codes = k_i8;
-    qa.q_scale = q_scale;
-    qa.k_scale = k_scale;
-    qa.BH = B * H;
-    qa.H = H;
-    qa.set_lengths(S, S);
-    qa.k_mean = k_mean;
-    e = launch_qk_quantize<int8_t>(qa, st);
+    const QKQuantArgs<int8_t> qa = public_args(q, k, B, S, H, q_i8, q_scale, k_i8, k_scale, k_mean);
+    e = launch_qkv_quantize<int8_t>(qa, static_cast<const uint16_t*>(v), at<uint32_t>(scratch, sum_bytes), vt_fp8,
+                                    v_scale, st);
   }
-  if (e == cudaSuccess)
-    e = launch_v_quantize(static_cast<const uint16_t*>(v), B, S, H, padded_len(S),
-                          at<uint32_t>(scratch, sum_bytes), vt_fp8, v_scale, st);
   cudaError_t e2 = cudaFreeAsync(scratch, st);
   if (e != cudaSuccess) return cuda_fail(e, "quantisation launch");
   if (e2 != cudaSuccess) return cuda_fail(e2, "scratch release");
@@ -526,7 +518,7 @@ sage_status sage_debug_staging_codes(const void* q, const void* k, int B, int S,
   if (s != SAGE_OK) return s;
   const QKQuantArgs<__half> qa = staging_args(q, k, B, S, S, H, static_cast<__half*>(q16), q_scale,
                                               static_cast<__half*>(k16), k_scale, false, nullptr);
-  cudaError_t e = launch_qk_quantize<__half>(qa, static_cast<cudaStream_t>(stream));
+  cudaError_t e = launch_qkv_quantize<__half>(qa, nullptr, nullptr, nullptr, nullptr, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "Q/K quantisation launch");
   return SAGE_OK;
 }

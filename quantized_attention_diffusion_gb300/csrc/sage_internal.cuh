@@ -38,8 +38,14 @@ struct QKQuantArgs {
   }
 };
 
+// The quantisation of Q, K and V, in two launches: Q/K codes together with
+// the per-channel V maxima (amax_bits [B*H*128] scratch, zeroed here), then
+// the E4M3 V^T codes and scales (vt [B, H, 128, S_pad], v_scale [B, H, 128]).
+// V has the K length a.S[1].  With v == nullptr only the Q/K codes are made
+// (one launch; amax_bits, vt and v_scale unused).
 template <typename CodeT>
-cudaError_t launch_qk_quantize(const QKQuantArgs<CodeT>& a, cudaStream_t stream);
+cudaError_t launch_qkv_quantize(const QKQuantArgs<CodeT>& a, const uint16_t* v, uint32_t* amax_bits, uint8_t* vt,
+                                float* v_scale, cudaStream_t stream);
 
 // K smoothing: per-channel means of K over its S tokens, mean = fp32(sum / S)
 // with the sum exact (64-bit fixed point, 2^-40, for |k| in [2^-33, 2^23)).
@@ -47,9 +53,6 @@ cudaError_t launch_qk_quantize(const QKQuantArgs<CodeT>& a, cudaStream_t stream)
 cudaError_t launch_k_channel_means(const uint16_t* k, int B, int S, int H, unsigned long long* sums, float* mean,
                                    cudaStream_t stream);
 
-// V channel maxima (amax_bits [B*H*128], zeroed here) then E4M3 V^T codes.
-cudaError_t launch_v_quantize(const uint16_t* v, int B, int S, int H, int S_pad, uint32_t* amax_bits,
-                              uint8_t* vt, float* v_scale, cudaStream_t stream);
 
 cudaError_t launch_widen_codes(const int8_t* src, __half* dst, size_t n, cudaStream_t stream);
 
