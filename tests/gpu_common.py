@@ -96,7 +96,7 @@ def lse_tolerance(S, lse_ref, lse_ties):
     return steps * eps + 8 * eps * mag + np.asarray(lse_ties)
 
 
-def assert_within_two_pass_bound(got, quant, S, scale, rows, ties, what=""):
+def assert_within_two_pass_bound(got, quant, S, scale, rows, ties, what="", Skv=None):
     """The kernel's output against the oracle's two-pass form (one tile of
     all keys: no dependence on the kernel's 96-key tiling), within the
     derived bound of reading R16 plus what separates the kernel from the
@@ -105,19 +105,22 @@ def assert_within_two_pass_bound(got, quant, S, scale, rows, ties, what=""):
       |gpu - two_pass| <= spread_d * G       (tiled vs two-pass, R16)
                           + ties             (P codes on an E4M3 midpoint, R12)
                           + 2 BF16 ulps      (the two outputs' final roundings)
-                          + (S/32 + S/96 + 8) 2^-24 max_j |v_jd|
+                          + (Skv/32 + Skv/96 + 8) 2^-24 max_j |v_jd|
                                              (the kernel's fp32 accumulation:
-                                              S/32 MMA steps, S/96 rescales)
+                                              Skv/32 MMA steps, Skv/96 rescales)
 
-    got: float [n, D] for the rows (b, h, i).  Returns (max |gpu - two_pass|,
-    the largest fraction of the tolerance used)."""
+    S: query rows; Skv: keys and values (default S).  got: float [n, D] for
+    the rows (b, h, i).  Returns (max |gpu - two_pass|, the largest fraction
+    of the tolerance used)."""
+    Skv = S if Skv is None else int(Skv)
     rows = np.asarray(rows, dtype=np.int32).reshape(-1, 3)
-    two_pass = f32(oracle.attend_rows(quant, S, scale, rows, kv_tile=oracle.TWO_PASS)).astype(np.float64)
-    G = oracle.requant_bound(quant, S, scale, rows, kv_tile=oracle.KV_TILE)
-    spread = oracle.v_spread(quant, S)[rows[:, 0], rows[:, 1]]
+    two_pass = f32(oracle.attend_rows(quant, S, scale, rows, kv_tile=oracle.TWO_PASS,
+                                      Skv=Skv)).astype(np.float64)
+    G = oracle.requant_bound(quant, S, scale, rows, kv_tile=oracle.KV_TILE, Skv=Skv)
+    spread = oracle.v_spread(quant, Skv)[rows[:, 0], rows[:, 1]]
     vt, vs = quant[4], quant[5]
-    vmaxabs = (np.abs(oracle.e4m3_decode(vt[..., :S])).max(axis=-1) * vs.astype(np.float64))
-    noise = (S / 32 + S / 96 + 8) * 2.0 ** -24 * vmaxabs[rows[:, 0], rows[:, 1]]
+    vmaxabs = (np.abs(oracle.e4m3_decode(vt[..., :Skv])).max(axis=-1) * vs.astype(np.float64))
+    noise = (Skv / 32 + Skv / 96 + 8) * 2.0 ** -24 * vmaxabs[rows[:, 0], rows[:, 1]]
     got = np.asarray(got, dtype=np.float64)
     tol = (spread * G[:, None] + np.asarray(ties)[:, None] + noise
            + 2 * bf16_ulp(np.maximum(np.abs(got), np.abs(two_pass))))

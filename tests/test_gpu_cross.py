@@ -11,7 +11,8 @@ import torch
 
 import oracle
 from quantized_attention_diffusion_gb300.workloads import WORKLOADS, bf16_bits, make_qkv, make_workload
-from tests.gpu_common import (COS_BAR, assert_close_to_oracle, cosine, default_scale, ensure_library, f32,
+from tests.gpu_common import (COS_BAR, assert_close_to_oracle, assert_within_two_pass_bound, cosine,
+                              default_scale, ensure_library, f32,
                               lse_tolerance)
 
 pytestmark = pytest.mark.gpu
@@ -45,6 +46,7 @@ def _check(out, lse, bits, Sq, Skv, scale, rows, what):
                                                           return_lse=True, Skv=Skv)
     got = out[rows[:, 0], rows[:, 2], rows[:, 1]]
     err, _ = assert_close_to_oracle(got, f32(ref_bits), ties, what)
+    assert_within_two_pass_bound(got, quant, Sq, scale, rows, ties, what + " vs two-pass", Skv=Skv)
     lse_got = lse[rows[:, 0], rows[:, 1], rows[:, 2]].astype(np.float64)
     lerr = np.abs(lse_got - lse_ref)
     tol = lse_tolerance(Skv, lse_ref, lse_tie)

@@ -223,3 +223,24 @@ def test_tie_bound_value_at_an_e4m3_midpoint():
     quant_off, scale_off = _midpoint_row(8.4)
     _, ties_off = oracle.attend_rows(quant_off, 2, scale_off, rows, return_ties=True)
     assert ties_off[0] == 0.0
+
+
+def test_requant_bound_holds_for_cross_attention():
+    """Reading R14 with R16: a short query block against longer and shorter
+    key/value sequences (ragged lengths), every row, tiles 96 and 1."""
+    from quantized_attention_diffusion_gb300.workloads import make_qkv
+    for (Sq, Skv, seed) in [(40, 333, 60), (200, 97, 61)]:
+        q, k, v = [bf16_bits(t) for t in make_qkv(1, Sq, 2, recipe="k_channel_offset", seed=seed, Skv=Skv)]
+        quant = oracle.quantize(q, k, v)
+        rows = oracle.all_rows(1, Sq, 2)
+        scale = 1 / math.sqrt(128)
+        spread = oracle.v_spread(quant, Skv)[rows[:, 0], rows[:, 1]]
+        two_pass = f32(oracle.attend_rows(quant, Sq, scale, rows, kv_tile=oracle.TWO_PASS,
+                                          Skv=Skv)).astype(np.float64)
+        for tile in (96, 1):
+            tiled = f32(oracle.attend_rows(quant, Sq, scale, rows, kv_tile=tile, Skv=Skv)).astype(np.float64)
+            G = oracle.requant_bound(quant, Sq, scale, rows, kv_tile=tile, Skv=Skv)
+            bound = spread * G[:, None] + bf16_ulp(np.maximum(np.abs(tiled), np.abs(two_pass)))
+            assert np.all(np.abs(tiled - two_pass) <= bound), (Sq, Skv, tile)
+            if tile == 96 and Skv <= 96:
+                assert np.all(G == 0) and np.array_equal(tiled, two_pass)
