@@ -321,66 +321,105 @@ __device__ __forceinline__ uint16_t e4m3_code2(float x0, float x1, float sv0, fl
 }
 
 // Encode one 128-token tile of one (batch, head) and write it transposed.
-// grid = (S_pad / 128, B*H), 256 threads.  Warp w owns channels 16w .. +15;
-// its lane l owns channels 16w + 4*(l%4) .. +3 of tokens 16*(l/4) .. +15.  A
-// load instruction of the warp reads eight whole 32-byte sectors (16
-// channels of 8 tokens); after encoding, a 4x4 byte transpose in registers
-// gives each lane 16 tokens of each of its 4 channels, so a store
-// instruction writes 4 channel rows x 128 contiguous bytes.  All loads are
-// issued before any encoding.  Tokens >= S get code 0.
-__global__ void __launch_bounds__(256) v_encode_kernel(const uint16_t* __restrict__ v, int S, int H,
-                                                       int S_pad,
-                                                       const uint32_t* __restrict__ amax_bits,
-                                                       uint8_t* __restrict__ vt,
-                                                       float* __restrict__ v_scale) {
+// grid = (S_pad / 128, B*H), 256 threads.
+//   Load: warp w covers tile tokens 16w .. 16w+15; in load instruction i
+//   (0..7) lanes 0-15 read token 16w + i and lanes 16-31 token 16w + 8 + i,
+//   lane l channels 8(l%16) .. +7 (16 bytes): two whole 256-byte rows per
+//   instruction.  A lane so holds 8 consecutive tokens (token group tg =
+//   2w + l/16: tile tokens 8tg .. 8tg+7) of 8 channels.  Meanwhile threads
+//   0-127 form the 128 channel scales sv = fl(amax / 448) and fl(1 / sv)
+//   once, in shared memory.
+//   Transpose: each lane's 8 tokens x 8 channels of E4M3 codes are
+//   transposed in registers and stored, 8 bytes per channel, into a 128 x
+//   128-byte tile (channel rows); the 8-byte chunk of token group tg in
+//   channel row c sits at chunk tg ^ ((c / 8) % 16), so that the 32 stores of
+//   an instruction fall into distinct bank pairs twice (two wavefronts).
+//   Store: 8 lanes write one channel row's 128 contiguous bytes of V^T.
+// Tokens >= S get code 0.
+constexpr int kVEncThreads = 256;
+
+__global__ void __launch_bounds__(kVEncThreads, 4) v_encode_kernel(const uint16_t* __restrict__ v, int S, int H,
+                                                                   int S_pad,
+                                                                   const uint32_t* __restrict__ amax_bits,
+                                                                   uint8_t* __restrict__ vt,
+                                                                   float* __restrict__ v_scale) {
+  __shared__ __align__(16) uint8_t tile[kHeadDim * 128];
+  __shared__ __align__(16) float s_sv[kHeadDim];
+  __shared__ __align__(16) float s_rcp[kHeadDim];
+  __shared__ int s_fast[kHeadDim];
   const int bh = blockIdx.y, b = bh / H, h = bh % H;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int c4 = warp * 16 + (lane & 3) * 4;
-  const int s0 = blockIdx.x * 128 + (lane >> 2) * 16;
+  const int g = lane & 15;                 // channels 8g .. 8g+7
+  const int tg = 2 * warp + (lane >> 4);   // token group: tile tokens 8tg .. 8tg+7
+  const int s_tile = blockIdx.x * 128;
   const size_t tok_stride = static_cast<size_t>(H) * kHeadDim;
-  const uint16_t* src = v + (static_cast<size_t>(b) * S * H + h) * kHeadDim + c4;
-  uint2 raw[16];
+  const uint16_t* src = v + (static_cast<size_t>(b) * S * H + h) * kHeadDim + 8 * g;
+  uint4 raw[8];
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const int s = s0 + i;
-    raw[i] = s < S ? __ldcs(reinterpret_cast<const uint2*>(src + static_cast<size_t>(s) * tok_stride))
-                   : make_uint2(0, 0);
+  for (int i = 0; i < 8; ++i) {
+    const int s = s_tile + 8 * tg + i;
+    raw[i] = s < S ? __ldcs(reinterpret_cast<const uint4*>(src + static_cast<size_t>(s) * tok_stride))
+                   : make_uint4(0, 0, 0, 0);
   }
-  float sv[4];
+  if (threadIdx.x < kHeadDim) {
+    const int c = threadIdx.x;
+    const float sv = __fdiv_rn(__uint_as_float(amax_bits[static_cast<size_t>(bh) * kHeadDim + c]), 448.0f);
+    s_sv[c] = sv;
+    s_rcp[c] = __frcp_rn(sv);
+    s_fast[c] = sv >= 0x1p-125f && sv <= 0x1p125f;
+    if (blockIdx.x == 0) v_scale[static_cast<size_t>(bh) * kHeadDim + c] = sv;
+  }
+  __syncthreads();
+  float sv[8], rc[8];
   bool fast = true;
 #pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    sv[c] = __fdiv_rn(__uint_as_float(amax_bits[static_cast<size_t>(bh) * kHeadDim + c4 + c]), 448.0f);
-    fast &= sv[c] >= 0x1p-125f && sv[c] <= 0x1p125f;
+  for (int c = 0; c < 8; ++c) {
+    sv[c] = s_sv[8 * g + c];
+    rc[c] = s_rcp[8 * g + c];
+    fast &= s_fast[8 * g + c] != 0;
   }
-  const float2 rcp01 = make_float2(__frcp_rn(sv[0]), __frcp_rn(sv[1]));
-  const float2 rcp23 = make_float2(__frcp_rn(sv[2]), __frcp_rn(sv[3]));
-  if (blockIdx.x == 0 && (lane >> 2) == 0)
-    *reinterpret_cast<float4*>(v_scale + static_cast<size_t>(bh) * kHeadDim + c4) =
-        make_float4(sv[0], sv[1], sv[2], sv[3]);
-  uint32_t tok[16];   // tok[i]: the codes of token s0+i, channel c4+k in byte k
+  // tw[i][k]: token i's codes of channels 8g+4k .. +3 (channel in byte order)
+  uint32_t tw[8][2];
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const uint32_t lo = e4m3_code2(bf16_lo(raw[i].x), bf16_hi(raw[i].x), sv[0], sv[1], rcp01, fast);
-    const uint32_t hi = e4m3_code2(bf16_lo(raw[i].y), bf16_hi(raw[i].y), sv[2], sv[3], rcp23, fast);
-    tok[i] = lo | (hi << 16);
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t w[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const uint32_t lo = e4m3_code2(bf16_lo(w[2 * k]), bf16_hi(w[2 * k]), sv[4 * k], sv[4 * k + 1],
+                                     make_float2(rc[4 * k], rc[4 * k + 1]), fast);
+      const uint32_t hi = e4m3_code2(bf16_lo(w[2 * k + 1]), bf16_hi(w[2 * k + 1]), sv[4 * k + 2], sv[4 * k + 3],
+                                     make_float2(rc[4 * k + 2], rc[4 * k + 3]), fast);
+      tw[i][k] = lo | (hi << 16);
+    }
   }
-  uint32_t row[4][4];   // row[c][g]: tokens 4g..4g+3 of channel c4+c
+  // 4x4 byte transposes: cw[c][p] = tokens 4p .. 4p+3 of channel 8g + c.
+  uint32_t cw[8][2];
 #pragma unroll
-  for (int g = 0; g < 4; ++g) {
-    const uint32_t* w = tok + 4 * g;
-    const uint32_t a01 = __byte_perm(w[0], w[1], 0x5140), b01 = __byte_perm(w[0], w[1], 0x7362);
-    const uint32_t a23 = __byte_perm(w[2], w[3], 0x5140), b23 = __byte_perm(w[2], w[3], 0x7362);
-    row[0][g] = __byte_perm(a01, a23, 0x5410);
-    row[1][g] = __byte_perm(a01, a23, 0x7632);
-    row[2][g] = __byte_perm(b01, b23, 0x5410);
-    row[3][g] = __byte_perm(b01, b23, 0x7632);
+  for (int k = 0; k < 2; ++k) {
+#pragma unroll
+    for (int pp = 0; pp < 2; ++pp) {
+      const uint32_t w0 = tw[4 * pp][k], w1 = tw[4 * pp + 1][k], w2 = tw[4 * pp + 2][k], w3 = tw[4 * pp + 3][k];
+      const uint32_t a01 = __byte_perm(w0, w1, 0x5140), b01 = __byte_perm(w0, w1, 0x7362);
+      const uint32_t a23 = __byte_perm(w2, w3, 0x5140), b23 = __byte_perm(w2, w3, 0x7362);
+      cw[4 * k + 0][pp] = __byte_perm(a01, a23, 0x5410);
+      cw[4 * k + 1][pp] = __byte_perm(a01, a23, 0x7632);
+      cw[4 * k + 2][pp] = __byte_perm(b01, b23, 0x5410);
+      cw[4 * k + 3][pp] = __byte_perm(b01, b23, 0x7632);
+    }
   }
-  uint8_t* dst = vt + (static_cast<size_t>(bh) * kHeadDim + c4) * S_pad + s0;
 #pragma unroll
-  for (int c = 0; c < 4; ++c)
-    *reinterpret_cast<uint4*>(dst + static_cast<size_t>(c) * S_pad) =
-        make_uint4(row[c][0], row[c][1], row[c][2], row[c][3]);
+  for (int c = 0; c < 8; ++c)   // channel row 8g + c, swizzle (8g + c) / 8 % 16 = g
+    *reinterpret_cast<uint2*>(tile + (8 * g + c) * 128 + ((tg ^ g) << 3)) = make_uint2(cw[c][0], cw[c][1]);
+  __syncthreads();
+  const int m = threadIdx.x & 7;           // 16-byte piece m of a row: token groups 2m, 2m+1
+#pragma unroll
+  for (int it = 0; it < kHeadDim / (kVEncThreads / 8); ++it) {
+    const int c = it * (kVEncThreads / 8) + (threadIdx.x >> 3);
+    const int gc = (c >> 3) & 15;
+    uint4 x = *reinterpret_cast<const uint4*>(tile + c * 128 + (((2 * m) ^ (gc & 14)) << 3));
+    if (gc & 1) x = make_uint4(x.z, x.w, x.x, x.y);   // the pair's two 8-byte chunks were swapped
+    *reinterpret_cast<uint4*>(vt + (static_cast<size_t>(bh) * kHeadDim + c) * S_pad + s_tile + 16 * m) = x;
+  }
 }
 
 // int8 codes -> integer-valued fp16 codes, 16 per thread.
@@ -433,7 +472,8 @@ cudaError_t launch_qkv_quantize(const QKQuantArgs<CodeT>& a, const uint16_t* v, 
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || v == nullptr) return e;
   const int S_pad = a.S_pad[1];
-  v_encode_kernel<<<dim3(S_pad / 128, a.BH), 256, 0, stream>>>(v, a.S[1], a.H, S_pad, amax_bits, vt, v_scale);
+  v_encode_kernel<<<dim3(S_pad / 128, a.BH), kVEncThreads, 0, stream>>>(v, a.S[1], a.H, S_pad, amax_bits, vt,
+                                                                         v_scale);
   return cudaGetLastError();
 }
 template cudaError_t launch_qkv_quantize<int8_t>(const QKQuantArgs<int8_t>&, const uint16_t*, uint32_t*, uint8_t*,
