@@ -304,20 +304,10 @@ __global__ void k_mean_kernel(const unsigned long long* __restrict__ sums, int S
   }
 }
 
-// E4M3 codes of x0 / sv0 and x1 / sv1 (low byte first), bit-identical to
-// converting the correctly rounded quotients.  With rcp = fl(1/sv) for sv in
-// [2^-125, 2^125], y = x * rcp lies within 3 * 2^-24 relative of fl(x / sv),
-// so y (1 - 2^-20) and y (1 + 2^-20) bracket it; the conversion is monotonic,
-// so equal codes at both ends are the code of fl(x / sv).  Otherwise divide.
-__device__ __forceinline__ uint16_t e4m3_code2(float x0, float x1, float sv0, float sv1, float2 rcp, bool fast) {
-  if (fast) {
-    const float2 y = fmul2v(make_float2(x0, x1), rcp);
-    const float2 lo = fmul2v(y, make_float2(1.0f - 0x1p-20f, 1.0f - 0x1p-20f));
-    const float2 hi = fmul2v(y, make_float2(1.0f + 0x1p-20f, 1.0f + 0x1p-20f));
-    const uint16_t c_lo = cvt_e4m3x2(lo.x, lo.y), c_hi = cvt_e4m3x2(hi.x, hi.y);
-    if (c_lo == c_hi) return c_lo;
-  }
-  return cvt_e4m3x2(sv0 == 0.0f ? 0.0f : __fdiv_rn(x0, sv0), sv1 == 0.0f ? 0.0f : __fdiv_rn(x1, sv1));
+// E4M3 code of fl(x / sv) by the division itself (0 for sv = 0, where every
+// value of the channel is zero): the path for a scale outside [2^-100, 2^125].
+__device__ __forceinline__ uint8_t e4m3_code_div(float x, float sv) {
+  return static_cast<uint8_t>(cvt_e4m3x2(sv == 0.0f ? 0.0f : __fdiv_rn(x, sv), 0.0f));
 }
 
 // Encode one 128-token tile of one (batch, head) and write it transposed.
@@ -327,13 +317,27 @@ __device__ __forceinline__ uint16_t e4m3_code2(float x0, float x1, float sv0, fl
 //   lane l channels 8(l%16) .. +7 (16 bytes): two whole 256-byte rows per
 //   instruction.  A lane so holds 8 consecutive tokens (token group tg =
 //   2w + l/16: tile tokens 8tg .. 8tg+7) of 8 channels.  Meanwhile threads
-//   0-127 form the 128 channel scales sv = fl(amax / 448) and fl(1 / sv)
-//   once, in shared memory.
+//   0-127 form the 128 channel scales sv = fl(amax / 448) and nr =
+//   -fl(1/sv) once, in shared memory.
+//   Codes: the quotient's correction step of Markstein (IBM J. Res. Dev.
+//   34(1), 1990: a faithful quotient, its exact residual by one FMA and a
+//   second FMA with the correctly rounded reciprocal give the correctly
+//   rounded quotient), with the reciprocal negated:
+//     z = fl(x nr),  r = fma(z, sv, x),  y = fma(r, nr, z)  =  -fl(x / sv),
+//   zeros included (y = -0 for x = +0 and +0 for x = -0), and the E4M3 code
+//   of fl(x / sv) is the code of y with its sign bit flipped.  This holds
+//   for every bf16 x with |x| <= amax and every bf16 amax whose scale lies
+//   in [2^-100, 2^125] (every such pair has been checked against the
+//   division); a channel outside that range (an all-zero channel, or one
+//   whose values are all below ~2^-91) is re-encoded by the division after
+//   the tile is written.  Three packed FP32 operations and one paired
+//   conversion per two values, no compare and no branch.
 //   Transpose: each lane's 8 tokens x 8 channels of E4M3 codes are
 //   transposed in registers and stored, 8 bytes per channel, into a 128 x
 //   128-byte tile (channel rows); the 8-byte chunk of token group tg in
-//   channel row c sits at chunk tg ^ ((c / 8) % 16), so that the 32 stores of
-//   an instruction fall into distinct bank pairs twice (two wavefronts).
+//   channel row c sits at chunk tg ^ ((c / 8) % 16 & ~1), so that the 32
+//   stores of an instruction fall into distinct bank pairs twice (two
+//   wavefronts) and token groups 2m, 2m+1 stay one ordered 16-byte piece.
 //   Store: 8 lanes write one channel row's 128 contiguous bytes of V^T.
 // Tokens >= S get code 0.
 constexpr int kVEncThreads = 256;
@@ -345,38 +349,35 @@ __global__ void __launch_bounds__(kVEncThreads, 4) v_encode_kernel(const uint16_
                                                                    float* __restrict__ v_scale) {
   __shared__ __align__(16) uint8_t tile[kHeadDim * 128];
   __shared__ __align__(16) float s_sv[kHeadDim];
-  __shared__ __align__(16) float s_rcp[kHeadDim];
-  __shared__ int s_fast[kHeadDim];
+  __shared__ __align__(16) float s_nr[kHeadDim];
+  __shared__ __align__(16) int s_out[kHeadDim];   // scale outside [2^-100, 2^125]
   const int bh = blockIdx.y, b = bh / H, h = bh % H;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane & 15;                 // channels 8g .. 8g+7
   const int tg = 2 * warp + (lane >> 4);   // token group: tile tokens 8tg .. 8tg+7
-  const int s_tile = blockIdx.x * 128;
+  const int s0 = blockIdx.x * 128 + 8 * tg;
   const size_t tok_stride = static_cast<size_t>(H) * kHeadDim;
-  const uint16_t* src = v + (static_cast<size_t>(b) * S * H + h) * kHeadDim + 8 * g;
+  const uint16_t* src = v + (static_cast<size_t>(b) * S * H + h) * kHeadDim + 8 * g + static_cast<size_t>(s0) * tok_stride;
   uint4 raw[8];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int s = s_tile + 8 * tg + i;
-    raw[i] = s < S ? __ldcs(reinterpret_cast<const uint4*>(src + static_cast<size_t>(s) * tok_stride))
-                   : make_uint4(0, 0, 0, 0);
-  }
+  for (int i = 0; i < 8; ++i)
+    raw[i] = s0 + i < S ? __ldcs(reinterpret_cast<const uint4*>(src + i * tok_stride)) : make_uint4(0, 0, 0, 0);
   if (threadIdx.x < kHeadDim) {
     const int c = threadIdx.x;
     const float sv = __fdiv_rn(__uint_as_float(amax_bits[static_cast<size_t>(bh) * kHeadDim + c]), 448.0f);
     s_sv[c] = sv;
-    s_rcp[c] = __frcp_rn(sv);
-    s_fast[c] = sv >= 0x1p-125f && sv <= 0x1p125f;
+    s_nr[c] = -__frcp_rn(sv);
+    s_out[c] = !(sv >= 0x1p-100f && sv <= 0x1p125f);
     if (blockIdx.x == 0) v_scale[static_cast<size_t>(bh) * kHeadDim + c] = sv;
   }
   __syncthreads();
-  float sv[8], rc[8];
-  bool fast = true;
+  float sv[8], nr[8];
+  uint32_t out_of_range = 0;               // bit c: channel 8g + c takes the division
 #pragma unroll
   for (int c = 0; c < 8; ++c) {
     sv[c] = s_sv[8 * g + c];
-    rc[c] = s_rcp[8 * g + c];
-    fast &= s_fast[8 * g + c] != 0;
+    nr[c] = s_nr[8 * g + c];
+    out_of_range |= static_cast<uint32_t>(s_out[8 * g + c] != 0) << c;
   }
   // tw[i][k]: token i's codes of channels 8g+4k .. +3 (channel in byte order)
   uint32_t tw[8][2];
@@ -385,11 +386,14 @@ __global__ void __launch_bounds__(kVEncThreads, 4) v_encode_kernel(const uint16_
     const uint32_t w[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
-      const uint32_t lo = e4m3_code2(bf16_lo(w[2 * k]), bf16_hi(w[2 * k]), sv[4 * k], sv[4 * k + 1],
-                                     make_float2(rc[4 * k], rc[4 * k + 1]), fast);
-      const uint32_t hi = e4m3_code2(bf16_lo(w[2 * k + 1]), bf16_hi(w[2 * k + 1]), sv[4 * k + 2], sv[4 * k + 3],
-                                     make_float2(rc[4 * k + 2], rc[4 * k + 3]), fast);
-      tw[i][k] = lo | (hi << 16);
+      const float2 x0 = make_float2(bf16_lo(w[2 * k]), bf16_hi(w[2 * k]));
+      const float2 x1 = make_float2(bf16_lo(w[2 * k + 1]), bf16_hi(w[2 * k + 1]));
+      const float2 n0 = make_float2(nr[4 * k], nr[4 * k + 1]), n1 = make_float2(nr[4 * k + 2], nr[4 * k + 3]);
+      const float2 z0 = fmul2v(x0, n0), z1 = fmul2v(x1, n1);
+      const float2 r0 = ffma2v(z0, make_float2(sv[4 * k], sv[4 * k + 1]), x0);
+      const float2 r1 = ffma2v(z1, make_float2(sv[4 * k + 2], sv[4 * k + 3]), x1);
+      const float2 y0 = ffma2v(r0, n0, z0), y1 = ffma2v(r1, n1, z1);
+      tw[i][k] = cvt_e4m3x4(y0.x, y0.y, y1.x, y1.y) ^ 0x80808080u;
     }
   }
   // 4x4 byte transposes: cw[c][p] = tokens 4p .. 4p+3 of channel 8g + c.
@@ -407,18 +411,30 @@ __global__ void __launch_bounds__(kVEncThreads, 4) v_encode_kernel(const uint16_
       cw[4 * k + 3][pp] = __byte_perm(b01, b23, 0x7632);
     }
   }
+  uint8_t* my_chunk = tile + 8 * g * 128 + ((tg ^ (g & 14)) << 3);   // channel row 8g; + c * 128 for row 8g + c
 #pragma unroll
-  for (int c = 0; c < 8; ++c)   // channel row 8g + c, swizzle (8g + c) / 8 % 16 = g
-    *reinterpret_cast<uint2*>(tile + (8 * g + c) * 128 + ((tg ^ g) << 3)) = make_uint2(cw[c][0], cw[c][1]);
+  for (int c = 0; c < 8; ++c)   // channel row 8g + c, swizzle (8g + c) / 8 % 16 & ~1 = g & 14
+    *reinterpret_cast<uint2*>(my_chunk + c * 128) = make_uint2(cw[c][0], cw[c][1]);
+  if (__builtin_expect(out_of_range != 0u, 0)) {
+    // Re-encode this lane's out-of-range channels by the division: it reads
+    // its tokens again and overwrites its own bytes of the tile.
+    for (int i = 0; i < 8; ++i) {
+      const uint4 r = s0 + i < S ? *reinterpret_cast<const uint4*>(src + i * tok_stride) : make_uint4(0, 0, 0, 0);
+      const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        if ((out_of_range >> c) & 1u)
+          my_chunk[c * 128 + i] = e4m3_code_div((c & 1) ? bf16_hi(w[c >> 1]) : bf16_lo(w[c >> 1]), sv[c]);
+    }
+  }
   __syncthreads();
   const int m = threadIdx.x & 7;           // 16-byte piece m of a row: token groups 2m, 2m+1
 #pragma unroll
   for (int it = 0; it < kHeadDim / (kVEncThreads / 8); ++it) {
     const int c = it * (kVEncThreads / 8) + (threadIdx.x >> 3);
     const int gc = (c >> 3) & 15;
-    uint4 x = *reinterpret_cast<const uint4*>(tile + c * 128 + (((2 * m) ^ (gc & 14)) << 3));
-    if (gc & 1) x = make_uint4(x.z, x.w, x.x, x.y);   // the pair's two 8-byte chunks were swapped
-    *reinterpret_cast<uint4*>(vt + (static_cast<size_t>(bh) * kHeadDim + c) * S_pad + s_tile + 16 * m) = x;
+    const uint4 x = *reinterpret_cast<const uint4*>(tile + c * 128 + ((m ^ (gc >> 1)) << 4));
+    *reinterpret_cast<uint4*>(vt + (static_cast<size_t>(bh) * kHeadDim + c) * S_pad + blockIdx.x * 128 + 16 * m) = x;
   }
 }
 

@@ -76,7 +76,9 @@ def test_quantize_bit_exact(B, S, H, recipe, seed):
 
 def test_quantize_special_values_bit_exact():
     """Zero blocks and channels, constant channels, tiny (subnormal-scale) and
-    huge values, negative zeros, exact .5 quotients."""
+    huge values, negative zeros, exact .5 quotients; V channels whose scale
+    lies below 2^-100 (the encoder's division path), just above it, and an
+    all-negative-zero channel."""
     B, S, H = 1, 200, 2
     rng = np.random.default_rng(5)
     x = rng.normal(0, 1, size=(B, S, H, 128)).astype(np.float32)
@@ -87,6 +89,9 @@ def test_quantize_special_values_bit_exact():
     x[0, :, 1, 7] = 0.0                                # an all-zero V channel
     x[0, :, 0, 9] = 3500.0                             # the pages' V ~ 3500 channel
     x[0, 130, 0, :4] = [127.0, 63.5, -0.5, 1.5]        # halves after scale 1
+    x[0, :, 1, 11] *= 1e-35                            # V scale ~2^-123: division path
+    x[0, :, 1, 13] *= 1e-27                            # V scale ~2^-97: corrected quotient
+    x[0, :, 0, 20] = -0.0                              # V scale 0 from negative zeros
     t = torch.from_numpy(x).to(torch.bfloat16)
     bits = [oracle_bits(t)] * 3
     ref = oracle.quantize(*bits)

@@ -31,10 +31,12 @@ def v_encode_accesses(B, S, H):
     128 x + 8 tg + i (tg = 2w + l/16; only tokens < S) at channels
     8g .. 8g+7 (g = l % 16, 16 bytes); the register transposes give channel
     8g + c the tokens 8 tg .. 8 tg + 7, stored as 8 bytes at
-    tile[(8g + c) * 128 + 8 (tg ^ g)]; thread t then reads, for it = 0..3,
-    channel row c = 32 it + t/8, 16 bytes at 8 ((2m) ^ (gc & 14)) (m = t % 8,
-    gc = (c / 8) % 16), swaps the two 8-byte halves when gc is odd, and
-    writes them to V^T row (bh, c) at tokens 128 x + 16 m .. +15.  Checks
+    tile[(8g + c) * 128 + 8 (tg ^ (g & 14))]; thread t then reads, for
+    it = 0..3, channel row c = 32 it + t/8, 16 bytes at 16 (m ^ (gc / 2))
+    (m = t % 8, gc = (c / 8) % 16) and writes them to V^T row (bh, c) at
+    tokens 128 x + 16 m .. +15.  A lane with an out-of-range channel scale
+    rewrites byte i of its chunk in row 8g + c (c = 0..7, i = 0..7): those
+    are bytes the same lane stored.  Checks
     bounds, alignment, that every tile byte is written once and every V^T
     byte once, that V^T gets the transpose of the tokens' codes, and that
     each tile store instruction takes two bank wavefronts."""
@@ -53,23 +55,28 @@ def v_encode_accesses(B, S, H):
                     if s < S:
                         elem = ((b * S + s) * H + h) * D + 8 * g
                         assert elem % 8 == 0 and 0 <= elem and elem + 8 <= B * S * H * D
+                mine = set()
                 for c in range(8):
-                    addr = (8 * g + c) * 128 + ((tg ^ g) << 3)
+                    addr = (8 * g + c) * 128 + ((tg ^ (g & 14)) << 3)
                     assert addr % 8 == 0 and 0 <= addr and addr + 8 <= D * 128
                     for j in range(8):
                         assert tile[addr + j] == -1, "tile byte written twice"
                         tile[addr + j] = (128 * x + 8 * tg + j) * D + 8 * g + c
+                        mine.add(addr + j)
+                chunk = 8 * g * 128 + ((tg ^ (g & 14)) << 3)
+                for c in range(8):
+                    for i in range(8):
+                        assert chunk + c * 128 + i in mine          # division rewrite of its own byte
+                        assert tile[chunk + c * 128 + i] == (128 * x + 8 * tg + i) * D + 8 * g + c
             assert np.all(tile >= 0)
             for t in range(256):
                 m = t & 7
                 for it in range(4):
                     c = it * 32 + (t >> 3)
                     gc = (c >> 3) & 15
-                    a = c * 128 + (((2 * m) ^ (gc & 14)) << 3)
+                    a = c * 128 + ((m ^ (gc >> 1)) << 4)
                     assert a % 16 == 0 and a + 16 <= D * 128
-                    piece = tile[a:a + 16].copy()
-                    if gc & 1:
-                        piece = np.concatenate([piece[8:], piece[:8]])
+                    piece = tile[a:a + 16]
                     dst = (bh * D + c) * Sp + 128 * x + 16 * m
                     assert dst % 16 == 0 and dst + 16 <= BH * D * Sp
                     assert np.all(written[dst:dst + 16] == -1), "V^T byte written twice"
@@ -81,7 +88,7 @@ def v_encode_accesses(B, S, H):
     # bank wavefronts of one tile store instruction (fixed c) of warp w: 32 lanes x 8 bytes
     for w in range(8):
         for c in range(8):
-            pairs = [(((8 * (l & 15) + c) * 128 + (((2 * w + (l >> 4)) ^ (l & 15)) << 3)) // 8) % 16
+            pairs = [(((8 * (l & 15) + c) * 128 + (((2 * w + (l >> 4)) ^ (l & 14)) << 3)) // 8) % 16
                      for l in range(32)]
             assert max(np.bincount(pairs, minlength=16)) == 2
 
