@@ -28,6 +28,17 @@ namespace {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
+// a * b + c elementwise on the packed FP32 pipe, one rounding per lane.
+__device__ __forceinline__ float2 ffma2v(float2 a, float2 b, float2 c) {
+  float2 r;
+  asm("{\n\t.reg .b64 x, y, z, w;\n\t"
+      "mov.b64 x, {%2, %3};\n\tmov.b64 y, {%4, %5};\n\tmov.b64 z, {%6, %7};\n\t"
+      "fma.rn.f32x2 w, x, y, z;\n\tmov.b64 {%0, %1}, w;\n\t}"
+      : "=f"(r.x), "=f"(r.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return r;
+}
+
 // Rounding and code stores without the XU pipe (int/half conversions and
 // frnd there cap this HBM-bound kernel): y + 1.5*2^23 - 1.5*2^23 is y rounded
 // to the nearest integer, ties to even, exactly for |y| < 2^22, and the low
