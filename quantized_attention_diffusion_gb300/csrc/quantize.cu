@@ -216,9 +216,16 @@ __device__ __forceinline__ void v_amax_slice(const uint16_t* __restrict__ v, int
   const size_t tok_stride = static_cast<size_t>(H) * kHeadDim;
   const uint16_t* src = v + (static_cast<size_t>(b) * S * H + h) * kHeadDim + c8;
   float m[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-  for (int s = s0 + r; s < s1; s += 16) {
-    const uint4 q = __ldcs(reinterpret_cast<const uint4*>(src + static_cast<size_t>(s) * tok_stride));
-    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+  uint4 raw[kVRowsPerCta / 16];            // all of this thread's (at most 16) tokens in flight at once
+#pragma unroll
+  for (int k = 0; k < kVRowsPerCta / 16; ++k) {
+    const int s = s0 + r + 16 * k;
+    raw[k] = s < s1 ? __ldcs(reinterpret_cast<const uint4*>(src + static_cast<size_t>(s) * tok_stride))
+                    : make_uint4(0, 0, 0, 0);
+  }
+#pragma unroll
+  for (int k = 0; k < kVRowsPerCta / 16; ++k) {
+    const uint32_t w[4] = {raw[k].x, raw[k].y, raw[k].z, raw[k].w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       m[2 * i] = fmaxf(m[2 * i], fabsf(bf16_lo(w[i])));
