@@ -178,6 +178,42 @@ sage_status sage_attn_fwd_cross(const void* q, const void* k, const void* v, voi
                                 int Sq, int Skv, int H, int D, float softmax_scale, void* stream);
 
 /*
+ * sage_plan -- one sage_attn_fwd_cross call (sage_attn_fwd when Sq == Skv
+ * and lse is NULL) fixed to its pointers and shape, recorded once as a CUDA
+ * graph and replayed by sage_plan_launch.  What it computes is that call's
+ * (issue #15014 and PR #15060, as sage_attn_fwd: Q/K per-32-row-block INT8,
+ * V per-channel FP8, attend); the plan only removes the per-call host work
+ * (argument checks, workspace allocation, tensor-map encoding and the
+ * separate launches) for shapes too small to hide it.  No counterpart on
+ * the pages.
+ *
+ * sage_plan_create: arguments as sage_attn_fwd_cross (device pointers,
+ *   layouts, lse optional), checked the same way; *plan receives the plan
+ *   (host object owned by the caller) or NULL on failure.  The plan owns
+ *   the workspace the call would otherwise take from the library's pool
+ *   (sage_workspace_bytes(B, S, H, D) bytes when Sq == Skv == S), allocated
+ *   here with cudaMalloc on the current device, and records the
+ *   launches on a private stream: nothing runs on the device during
+ *   creation.  The wait limit in force (sage_set_wait_timeout_ns) is the
+ *   one the plan's kernels use; the timing hook (sage_set_attention_events)
+ *   is not recorded.  Errors: INVALID_ARG (plan NULL, bad shape or scale),
+ *   MISALIGNED, NO_MEMORY (workspace), CUDA (capture or instantiation).
+ * sage_plan_launch: runs the recorded call on `stream` (a cudaStream_t as
+ *   void*; NULL = legacy default stream), reading q, k and v as they are at
+ *   that point of the stream and writing out (and lse).  The current device
+ *   must be the plan's.  Launches of one plan share its workspace, so they
+ *   must not overlap: issue them on one stream or order them.  Allocates
+ *   nothing.  Errors: INVALID_ARG (plan NULL, other device), CUDA.
+ * sage_plan_destroy: frees the plan and its workspace (cudaFree, which waits
+ *   for the device's outstanding work).  NULL is a no-op.  Errors: CUDA.
+ */
+typedef struct sage_plan sage_plan;
+sage_status sage_plan_create(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Sq,
+                             int Skv, int H, int D, float softmax_scale, sage_plan** plan);
+sage_status sage_plan_launch(sage_plan* plan, void* stream);
+sage_status sage_plan_destroy(sage_plan* plan);
+
+/*
  * sage_quantize_qkv_smooth_k -- sage_quantize_qkv with K smoothing: before K
  * is quantised, each (batch, head, channel) loses its mean over the S
  * tokens.  Passage: InvokeAI PR #9657, "Summary" / "How it works"

@@ -708,6 +708,11 @@ cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+cudaError_t load_attention_kernels() {
+  cudaFuncAttributes fa;
+  return cudaFuncGetAttributes(&fa, sage_attn_kernel<false, false>);
+}
+
 cudaError_t read_and_clear_device_error(int* code, cudaStream_t stream) {
   int host = 0;
   cudaError_t e = cudaMemcpyFromSymbolAsync(&host, g_sage_error, sizeof(int), 0, cudaMemcpyDeviceToHost, stream);

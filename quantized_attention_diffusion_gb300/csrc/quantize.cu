@@ -510,6 +510,13 @@ cudaError_t launch_qkv_quantize(const QKQuantArgs<CodeT>& a, const uint16_t* v, 
                                                                          v_scale);
   return cudaGetLastError();
 }
+cudaError_t load_quantize_kernels() {
+  cudaFuncAttributes fa;
+  cudaError_t e = cudaFuncGetAttributes(&fa, qkv_pass1_kernel<__half, false>);
+  if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, v_encode_kernel);
+  return e;
+}
+
 template cudaError_t launch_qkv_quantize<int8_t>(const QKQuantArgs<int8_t>&, const uint16_t*, uint32_t*, uint8_t*,
                                                  float*, cudaStream_t);
 template cudaError_t launch_qkv_quantize<__half>(const QKQuantArgs<__half>&, const uint16_t*, uint32_t*, uint8_t*,

@@ -9,6 +9,7 @@
 #include <cstdio>
 #include <cstring>
 #include <mutex>
+#include <new>
 #include <string>
 
 #include "sage.h"
@@ -318,6 +319,13 @@ sage_status check_workspace(void* ws, size_t bytes, int B, int S, int H) {
 
 }  // namespace
 
+// The host object behind sage_plan (opaque to callers).
+struct sage_plan {
+  int device;              // device the graph and workspace belong to
+  void* ws;                // cudaMalloc'd workspace the recorded launches use
+  cudaGraphExec_t exec;    // the recorded sage_attn_fwd_cross call
+};
+
 void sage::set_last_error(const char* fmt, ...) {
   char buf[512];
   va_list ap;
@@ -451,6 +459,96 @@ sage_status sage_attn_fwd_cross(const void* q, const void* k, const void* v, voi
   return with_pool_workspace(ws_layout(B, Sq, Skv, H).total, st, [&](void* ws) {
     return run_fused(q, k, v, out, B, Sq, Skv, H, softmax_scale, ws, st, lse);
   });
+}
+
+sage_status sage_plan_create(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Sq,
+                             int Skv, int H, int D, float softmax_scale, sage_plan** plan) {
+  if (!plan) return fail(SAGE_ERR_INVALID_ARG, "plan is NULL");
+  *plan = nullptr;
+  sage_status s = check_shape(B, Sq, H, D);
+  if (s == SAGE_OK) s = check_shape(B, Skv, H, D);
+  if (s == SAGE_OK) s = check_scale(softmax_scale);
+  if (s == SAGE_OK) s = check_ptrs({{q, "q"}, {k, "k"}, {v, "v"}, {out, "out"}});
+  if (s == SAGE_OK && lse) s = check_ptrs({{lse, "lse"}});
+  int dev = 0;
+  if (s == SAGE_OK) s = current_device(&dev);
+  if (s != SAGE_OK) return s;
+
+  const size_t bytes = ws_layout(B, Sq, Skv, H).total;
+  void* ws = nullptr;
+  cudaError_t e = fault_fires(SAGE_FAULT_POOL_ALLOC) ? cudaErrorMemoryAllocation : cudaMalloc(&ws, bytes);
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();
+    return fail(SAGE_ERR_NO_MEMORY, "plan workspace allocation of %zu bytes failed: %s", bytes, cudaGetErrorString(e));
+  }
+  cudaStream_t cs = nullptr;
+  cudaGraph_t graph = nullptr;
+  cudaGraphExec_t exec = nullptr;
+  e = load_quantize_kernels();                       // no module loading inside the capture
+  if (e == cudaSuccess) e = load_attention_kernels();
+  if (e != cudaSuccess) {
+    cudaFree(ws);
+    return cuda_fail(e, "plan kernel loading");
+  }
+  e = cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking);
+  if (e != cudaSuccess) {
+    cudaFree(ws);
+    return cuda_fail(e, "plan capture stream");
+  }
+  // Record the launches of the call; the timing hook stays out of the graph.
+  const cudaEvent_t before = t_attn_before, after = t_attn_after;
+  t_attn_before = t_attn_after = nullptr;
+  e = cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal);
+  if (e == cudaSuccess) {
+    s = run_fused(q, k, v, out, B, Sq, Skv, H, softmax_scale, ws, cs, lse);
+    const cudaError_t e_end = cudaStreamEndCapture(cs, &graph);   // ends the capture whatever happened
+    if (s == SAGE_OK && e_end != cudaSuccess) s = cuda_fail(e_end, "plan capture");
+  } else {
+    s = cuda_fail(e, "plan capture start");
+  }
+  t_attn_before = before;
+  t_attn_after = after;
+  if (s == SAGE_OK) {
+    e = cudaGraphInstantiate(&exec, graph, 0);
+    if (e != cudaSuccess) s = cuda_fail(e, "plan graph instantiation");
+  }
+  if (graph) cudaGraphDestroy(graph);
+  cudaStreamDestroy(cs);
+  sage_plan* p = nullptr;
+  if (s == SAGE_OK) {
+    p = new (std::nothrow) sage_plan{dev, ws, exec};
+    if (!p) s = fail(SAGE_ERR_NO_MEMORY, "plan object allocation failed");
+  }
+  if (s != SAGE_OK) {
+    if (exec) cudaGraphExecDestroy(exec);
+    cudaFree(ws);
+    return s;
+  }
+  *plan = p;
+  return SAGE_OK;
+}
+
+sage_status sage_plan_launch(sage_plan* plan, void* stream) {
+  if (!plan) return fail(SAGE_ERR_INVALID_ARG, "plan is NULL");
+  int dev = 0;
+  sage_status s = current_device(&dev);
+  if (s != SAGE_OK) return s;
+  if (dev != plan->device)
+    return fail(SAGE_ERR_INVALID_ARG, "plan was created on device %d, current device is %d", plan->device, dev);
+  if (fault_fires(SAGE_FAULT_ATTN_LAUNCH)) return fail(SAGE_ERR_CUDA, "plan launch: injected fault");
+  const cudaError_t e = cudaGraphLaunch(plan->exec, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "plan launch");
+  return SAGE_OK;
+}
+
+sage_status sage_plan_destroy(sage_plan* plan) {
+  if (!plan) return SAGE_OK;
+  cudaError_t e = cudaGraphExecDestroy(plan->exec);
+  const cudaError_t e2 = cudaFree(plan->ws);
+  delete plan;
+  if (e == cudaSuccess) e = e2;
+  if (e != cudaSuccess) return cuda_fail(e, "plan release");
+  return SAGE_OK;
 }
 
 sage_status sage_attn_fwd_quantized(const int8_t* q_i8, const float* q_scale, const int8_t* k_i8,

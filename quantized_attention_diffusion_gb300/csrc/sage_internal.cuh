@@ -78,6 +78,12 @@ struct AttnArgs {
 // Encodes the three TMA maps and launches the fused attention kernel.
 cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream);
 
+// Load the kernels the default attention path launches (the two quantisation
+// kernels and the attention kernel) into the current context, so that a
+// stream capture that launches them does not have to load a module.
+cudaError_t load_attention_kernels();
+cudaError_t load_quantize_kernels();
+
 // Records printf-style text as this thread's sage_last_error() message.
 void set_last_error(const char* fmt, ...);
 

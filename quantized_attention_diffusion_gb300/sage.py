@@ -36,7 +36,8 @@ EXPORTED = (
     "sage_quantize_qkv_noalloc", "sage_attn_fwd_lse", "sage_attn_fwd_cross",
     "sage_debug_fused_q", "sage_attn_fwd_fused_q", "sage_quantize_qkv_smooth_k",
     "sage_attn_fwd_smooth_k", "sage_attn_fwd_launches", "sage_debug_staging_codes",
-    "sage_debug_inject_fault", "sage_debug_pool_state",
+    "sage_debug_inject_fault", "sage_debug_pool_state", "sage_plan_create", "sage_plan_launch",
+    "sage_plan_destroy",
 )
 
 # Fault sites of sage_debug_inject_fault (include/sage.h).
@@ -78,6 +79,9 @@ def load_library(path: str = LIB_PATH):
             "sage_attn_fwd_ws": (S, [P, P, P, P, I, I, I, I, F, P, Z, P]),
             "sage_attn_fwd_lse": (S, [P, P, P, P, P, I, I, I, I, F, P]),
             "sage_attn_fwd_cross": (S, [P, P, P, P, P, I, I, I, I, I, F, P]),
+            "sage_plan_create": (S, [P, P, P, P, P, I, I, I, I, I, F, P]),
+            "sage_plan_launch": (S, [P, P]),
+            "sage_plan_destroy": (S, [P]),
             "sage_debug_fused_q": (S, [P, P, P, P, I, I, I, I, F, P, P, P]),
             "sage_attn_fwd_fused_q": (S, [P, P, P, P, I, I, I, I, F, P]),
             "sage_quantize_qkv_smooth_k": (S, [P, P, P, I, I, I, I, P, P, P, P, P, P, P, P]),
@@ -242,6 +246,73 @@ def attn_fwd_cross(q, k, v, softmax_scale: float | None = None, out=None, lse=No
                                        _ptr(lse) if lse is not None else None, B, Sq, Skv, H, D,
                                        float(softmax_scale), _stream(q.device)))
     return (out, lse) if lse is not None else out
+
+
+class Plan:
+    """One fixed attention call recorded as a CUDA graph (sage_plan_create):
+    q bf16 [B, Sq, H, 128], k and v bf16 [B, Skv, H, 128] (Skv = Sq for
+    self-attention), out bf16 [B, Sq, H, 128] and optionally lse fp32
+    [B, H, Sq], all fixed at creation.  ``launch()`` replays the call on the
+    current stream, reading q, k and v as they are then; launches of one plan
+    must not overlap (one stream, or ordered).  ``close()`` (or leaving a
+    ``with`` block) releases the graph and its workspace."""
+
+    def __init__(self, q, k, v, softmax_scale: float | None = None, out=None, lse=None):
+        lib = load_library()
+        for name, t in (("q", q), ("k", k), ("v", v)):
+            if not isinstance(t, torch.Tensor) or t.dtype != torch.bfloat16 or not t.is_cuda \
+                    or not t.is_contiguous() or t.dim() != 4:
+                raise ValueError(f"{name} must be a contiguous bf16 CUDA tensor [B, S, H, D]")
+        B, Sq, H, D = q.shape
+        if k.shape != v.shape or k.shape[0] != B or k.shape[2] != H or k.shape[3] != D:
+            raise ValueError(f"k and v must be [B, Skv, H, D] with B, H, D of q; got {tuple(k.shape)}, "
+                             f"{tuple(v.shape)} for q {tuple(q.shape)}")
+        if k.device != q.device or v.device != q.device:
+            raise ValueError("q, k and v must be on one device")
+        if softmax_scale is None:
+            softmax_scale = 1.0 / math.sqrt(D)
+        if out is None:
+            out = torch.empty_like(q)
+        if out.shape != q.shape or out.dtype != torch.bfloat16 or not out.is_contiguous() or out.device != q.device:
+            raise ValueError("out must be a contiguous bf16 tensor of q's shape on q's device")
+        if lse is not None and (lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, Sq)
+                                or not lse.is_contiguous() or lse.device != q.device):
+            raise ValueError("lse must be a contiguous float32 [B, H, Sq] tensor on q's device")
+        self.q, self.k, self.v, self.out, self.lse = q, k, v, out, lse   # kept alive with the graph
+        self.device = q.device
+        self._lib = lib
+        self._h = ctypes.c_void_p(0)
+        with torch.cuda.device(q.device):
+            _check(lib.sage_plan_create(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse) if lse is not None else None,
+                                        B, Sq, k.shape[1], H, D, float(softmax_scale), ctypes.byref(self._h)))
+
+    def launch(self):
+        if not self._h:
+            raise RuntimeError("plan is closed")
+        with torch.cuda.device(self.device):
+            _check(self._lib.sage_plan_launch(self._h, _stream(self.device)))
+        return self.out
+
+    def close(self):
+        if self._h:
+            with torch.cuda.device(self.device):
+                st = self._lib.sage_plan_destroy(self._h)
+            self._h = ctypes.c_void_p(0)
+            _check(st)
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def __del__(self):
+        try:
+            if self._h and self._lib is not None:
+                self._lib.sage_plan_destroy(self._h)
+                self._h = ctypes.c_void_p(0)
+        except Exception:
+            pass
 
 
 def debug_fused_q(q, k, v, softmax_scale: float | None = None):

@@ -146,3 +146,25 @@ def test_test_hooks_check_their_arguments_on_the_host(lib):
                                       P(FAKE), None)
     assert st == MISALIGNED
     assert b"k16" in lib.sage_last_error()
+
+
+def test_plan_checks_its_arguments_on_the_host(lib):
+    """sage_plan_create rejects what sage_attn_fwd_cross rejects, before any
+    CUDA call, and leaves *plan NULL; launch and destroy check for NULL."""
+    h = ctypes.c_void_p(FAKE)
+    args = (P(FAKE), P(FAKE), P(FAKE), P(FAKE), None)
+    assert lib.sage_plan_create(*args, 1, 256, 256, 2, 128, 0.1, None) == INVALID
+    assert lib.sage_plan_create(*args, 1, 256, 256, 2, 64, 0.1, ctypes.byref(h)) == UNSUPPORTED
+    assert h.value is None
+    h = ctypes.c_void_p(FAKE)
+    assert lib.sage_plan_create(*args, 1, 256, 0, 2, 128, 0.1, ctypes.byref(h)) == INVALID
+    assert h.value is None
+    assert lib.sage_plan_create(*args, 1, 256, 256, 2, 128, float("nan"), ctypes.byref(h)) == INVALID
+    assert lib.sage_plan_create(P(FAKE), P(FAKE), P(FAKE + 8), P(FAKE), None, 1, 256, 256, 2, 128, 0.1,
+                                ctypes.byref(h)) == MISALIGNED
+    assert b"v" in lib.sage_last_error()
+    assert lib.sage_plan_create(P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE + 4), 1, 256, 256, 2, 128, 0.1,
+                                ctypes.byref(h)) == MISALIGNED
+    assert b"lse" in lib.sage_last_error()
+    assert lib.sage_plan_launch(None, None) == INVALID
+    assert lib.sage_plan_destroy(None) == OK
