@@ -280,6 +280,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmQ);
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
+    // This thread is also the Q/K producer: Q and the first K stages go out
+    // now, while the rest of the block still sets up (their regions of shared
+    // memory are touched by nothing else before the block barrier).
+    mbar_arrive_expect_tx(&bars.q_full, 2 * kQTileBytes);
+    for (int t = 0; t < 2; ++t) {
+      if constexpr (kFuseQ) {   // bf16 [B, S, H, 128]: box of 64 channels x 128 tokens of one (b, h)
+        const int b = bh / p.H, h = bh % p.H;
+        tma_load_4d(sQ + t * kQTileBytes, &tmQ, &bars.q_full, 0, h, q_row0 + t * kTile, b);
+        tma_load_4d(sQ + t * kQTileBytes + kQHalf, &tmQ, &bars.q_full, 64, h, q_row0 + t * kTile, b);
+      } else {
+        tma_load_3d(sQ + t * kQTileBytes, &tmQ, &bars.q_full, 0, q_row0 + t * kTile, bh);
+        tma_load_3d(sQ + t * kQTileBytes + kQHalf, &tmQ, &bars.q_full, 64, q_row0 + t * kTile, bh);
+      }
+    }
+    for (int j = 0; j < kStages && j < p.n_kv; ++j) {
+      mbar_arrive_expect_tx(&bars.k_full[j], kKTileBytes);
+      tma_load_3d(sK + j * kKTileBytes, &tmK, &bars.k_full[j], 0, j * kKV, bh);
+      tma_load_3d(sK + j * kKTileBytes + kKHalf, &tmK, &bars.k_full[j], 64, j * kKV, bh);
+    }
   }
   if (threadIdx.x < kHeadDim) sv_smem[threadIdx.x] = p.v_scale[static_cast<size_t>(bh) * kHeadDim + threadIdx.x];
   if (warp == 2 || warp == 3) {
@@ -304,19 +323,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer --
     if (lane == 0) {
-      mbar_arrive_expect_tx(&bars.q_full, 2 * kQTileBytes);
-      for (int t = 0; t < 2; ++t) {
-        if constexpr (kFuseQ) {   // bf16 [B, S, H, 128]: box of 64 channels x 128 tokens of one (b, h)
-          const int b = bh / p.H, h = bh % p.H;
-          tma_load_4d(sQ + t * kQTileBytes, &tmQ, &bars.q_full, 0, h, q_row0 + t * kTile, b);
-          tma_load_4d(sQ + t * kQTileBytes + kQHalf, &tmQ, &bars.q_full, 64, h, q_row0 + t * kTile, b);
-        } else {
-          tma_load_3d(sQ + t * kQTileBytes, &tmQ, &bars.q_full, 0, q_row0 + t * kTile, bh);
-          tma_load_3d(sQ + t * kQTileBytes + kQHalf, &tmQ, &bars.q_full, 64, q_row0 + t * kTile, bh);
-        }
-      }
-      int k_issued = 0;
-      for (int j = 0; j < p.n_kv; ++j) {
+      // Q and the first kStages K stages were issued during set-up.
+      int k_issued = min(kStages, p.n_kv);
+      for (int j = k_issued; j < p.n_kv; ++j) {
         const int s = j % kStages, r = j / kStages;
         if (r > 0 && !wait_bar(&bars.k_empty[s], (r - 1) & 1, abort_v, p.timeout_ns)) break;
         mbar_arrive_expect_tx(&bars.k_full[s], kKTileBytes);
