@@ -25,6 +25,9 @@
  *   - Nothing traps on the device.  A device-side wait that runs past its
  *     limit records SAGE_ERR_TIMEOUT in a per-device error word, which
  *     sage_sync_status() reports.
+ *   - Pointers are 16-byte aligned; the `out` of every entry point that
+ *     runs the attention kernel is 32-byte aligned (the kernel writes each
+ *     output row as 32-byte vectors).  Otherwise SAGE_ERR_MISALIGNED.
  *   - Shapes: B, S, H >= 1; D must be 128.  B*H <= 2^31-1.
  *     S_pad = ceil(S / 128) * 128, nb = ceil(S / 32).
  */
@@ -42,7 +45,7 @@ typedef enum sage_status {
   SAGE_OK = 0,
   SAGE_ERR_INVALID_ARG = 1, /* a size < 1, a NULL pointer, a non-finite or non-positive scale */
   SAGE_ERR_UNSUPPORTED = 2, /* head dimension other than 128 */
-  SAGE_ERR_MISALIGNED = 3,  /* a pointer not 16-byte aligned */
+  SAGE_ERR_MISALIGNED = 3,  /* a pointer not 16-byte aligned (an attention `out` not 32-byte aligned) */
   SAGE_ERR_CUDA = 4,        /* a CUDA runtime or launch error (message kept) */
   SAGE_ERR_NO_MEMORY = 5,   /* workspace allocation failed */
   SAGE_ERR_TIMEOUT = 6,     /* a device wait gave up (reported by sage_sync_status) */

@@ -145,6 +145,20 @@ __device__ __forceinline__ void store_bf16x8(uint16_t* dst, const float (&v)[8])
   *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
 }
 
+// Sixteen floats -> sixteen bf16 (round to nearest even) in one 32-byte
+// store; dst must be 32-byte aligned.
+__device__ __forceinline__ void store_bf16x16(uint16_t* dst, const float (&v)[16]) {
+  uint32_t w[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    __nv_bfloat162 b = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+    w[i] = *reinterpret_cast<uint32_t*>(&b);
+  }
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(w[0]), "r"(w[1]),
+               "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
+}
+
 // One row's 96 integer scores -> 96 E4M3 probabilities p~ = e4m3(2^(acc *
 // cb[block] - bias)), four codes per word, key k in byte k%4 of word k/4.
 __device__ __forceinline__ void softmax_p(const float (&a)[kKV], const float (&cb)[3], float bias,
@@ -582,14 +596,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld_wait();
         if (row_valid) {
 #pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            float v8[8];
+          for (int g = 0; g < 2; ++g) {
+            float v16[16];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const int d = c * 32 + g * 8 + e;
-              v8[e] = __uint_as_float(o[g * 8 + e]) * (sv_smem[d] * inv_l);
+            for (int e = 0; e < 16; ++e) {
+              const int d = c * 32 + g * 16 + e;
+              v16[e] = __uint_as_float(o[g * 16 + e]) * (sv_smem[d] * inv_l);
             }
-            store_bf16x8(orow + c * 32 + g * 8, v8);
+            store_bf16x16(orow + c * 32 + g * 16, v16);
           }
         }
       }

@@ -63,6 +63,12 @@ sage_status check_ptrs(std::initializer_list<std::pair<const void*, const char*>
   return SAGE_OK;
 }
 
+// The attention kernel writes each output row as 32-byte vectors.
+sage_status check_out(const void* out) {
+  if (!aligned(out, 32)) return fail(SAGE_ERR_MISALIGNED, "out is not 32-byte aligned");
+  return SAGE_OK;
+}
+
 // Workspace layout (all offsets 256-byte aligned).
 struct WsLayout {
   size_t q16, k16, vt, qs, ks, vs, vamax, ksum, kmean, total;
@@ -405,6 +411,7 @@ sage_status sage_attn_fwd_smooth_k(const void* q, const void* k, const void* v, 
   sage_status s = check_shape(B, S, H, D);
   if (s == SAGE_OK) s = check_scale(softmax_scale);
   if (s == SAGE_OK) s = check_ptrs({{q, "q"}, {k, "k"}, {v, "v"}, {out, "out"}});
+  if (s == SAGE_OK) s = check_out(out);
   if (s != SAGE_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   return with_pool_workspace(ws_layout(B, S, S, H).total, st, [&](void* ws) {
@@ -418,6 +425,7 @@ sage_status sage_attn_fwd_ws(const void* q, const void* k, const void* v, void* 
   sage_status s = check_shape(B, S, H, D);
   if (s == SAGE_OK) s = check_scale(softmax_scale);
   if (s == SAGE_OK) s = check_ptrs({{q, "q"}, {k, "k"}, {v, "v"}, {out, "out"}});
+  if (s == SAGE_OK) s = check_out(out);
   if (s == SAGE_OK) s = check_workspace(workspace, workspace_bytes, B, S, H);
   if (s != SAGE_OK) return s;
   return run_fused(q, k, v, out, B, S, S, H, softmax_scale, workspace, static_cast<cudaStream_t>(stream));
@@ -428,6 +436,7 @@ sage_status sage_attn_fwd(const void* q, const void* k, const void* v, void* out
   sage_status s = check_shape(B, S, H, D);
   if (s == SAGE_OK) s = check_scale(softmax_scale);
   if (s == SAGE_OK) s = check_ptrs({{q, "q"}, {k, "k"}, {v, "v"}, {out, "out"}});
+  if (s == SAGE_OK) s = check_out(out);
   if (s != SAGE_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   return with_pool_workspace(ws_layout(B, S, S, H).total, st, [&](void* ws) {
@@ -440,6 +449,7 @@ sage_status sage_attn_fwd_lse(const void* q, const void* k, const void* v, void*
   sage_status s = check_shape(B, S, H, D);
   if (s == SAGE_OK) s = check_scale(softmax_scale);
   if (s == SAGE_OK) s = check_ptrs({{q, "q"}, {k, "k"}, {v, "v"}, {out, "out"}, {lse, "lse"}});
+  if (s == SAGE_OK) s = check_out(out);
   if (s != SAGE_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   return with_pool_workspace(ws_layout(B, S, S, H).total, st, [&](void* ws) {
@@ -453,6 +463,7 @@ sage_status sage_attn_fwd_cross(const void* q, const void* k, const void* v, voi
   if (s == SAGE_OK) s = check_shape(B, Skv, H, D);
   if (s == SAGE_OK) s = check_scale(softmax_scale);
   if (s == SAGE_OK) s = check_ptrs({{q, "q"}, {k, "k"}, {v, "v"}, {out, "out"}});
+  if (s == SAGE_OK) s = check_out(out);
   if (s == SAGE_OK && lse) s = check_ptrs({{lse, "lse"}});
   if (s != SAGE_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -469,6 +480,7 @@ sage_status sage_plan_create(const void* q, const void* k, const void* v, void* 
   if (s == SAGE_OK) s = check_shape(B, Skv, H, D);
   if (s == SAGE_OK) s = check_scale(softmax_scale);
   if (s == SAGE_OK) s = check_ptrs({{q, "q"}, {k, "k"}, {v, "v"}, {out, "out"}});
+  if (s == SAGE_OK) s = check_out(out);
   if (s == SAGE_OK && lse) s = check_ptrs({{lse, "lse"}});
   int dev = 0;
   if (s == SAGE_OK) s = current_device(&dev);
@@ -561,6 +573,7 @@ sage_status sage_attn_fwd_quantized(const int8_t* q_i8, const float* q_scale, co
   if (s == SAGE_OK)
     s = check_ptrs({{q_i8, "q_i8"}, {q_scale, "q_scale"}, {k_i8, "k_i8"}, {k_scale, "k_scale"},
                     {vt_fp8, "vt_fp8"}, {v_scale, "v_scale"}, {out, "out"}});
+  if (s == SAGE_OK) s = check_out(out);
   if (s == SAGE_OK) s = check_workspace(workspace, workspace_bytes, B, S, H);
   if (s != SAGE_OK) return s;
   return run_quantized(q_i8, q_scale, k_i8, k_scale, vt_fp8, v_scale, out, nullptr, B, S, H, softmax_scale,
@@ -577,6 +590,7 @@ sage_status sage_debug_qk_int32(const int8_t* q_i8, const float* q_scale, const 
   if (s == SAGE_OK)
     s = check_ptrs({{q_i8, "q_i8"}, {q_scale, "q_scale"}, {k_i8, "k_i8"}, {k_scale, "k_scale"},
                     {vt_fp8, "vt_fp8"}, {v_scale, "v_scale"}, {out, "out"}, {s_out, "s_out"}});
+  if (s == SAGE_OK) s = check_out(out);
   if (s == SAGE_OK) s = check_workspace(workspace, workspace_bytes, B, S, H);
   if (s != SAGE_OK) return s;
   return run_quantized(q_i8, q_scale, k_i8, k_scale, vt_fp8, v_scale, out, s_out, B, S, H, softmax_scale,
@@ -588,6 +602,7 @@ sage_status sage_attn_fwd_fused_q(const void* q, const void* k, const void* v, v
   sage_status s = check_shape(B, S, H, D);
   if (s == SAGE_OK) s = check_scale(softmax_scale);
   if (s == SAGE_OK) s = check_ptrs({{q, "q"}, {k, "k"}, {v, "v"}, {out, "out"}});
+  if (s == SAGE_OK) s = check_out(out);
   if (s != SAGE_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   return with_pool_workspace(ws_layout(B, S, S, H).total, st, [&](void* ws) {
@@ -601,6 +616,7 @@ sage_status sage_debug_fused_q(const void* q, const void* k, const void* v, void
   if (s == SAGE_OK) s = check_scale(softmax_scale);
   if (s == SAGE_OK)
     s = check_ptrs({{q, "q"}, {k, "k"}, {v, "v"}, {out, "out"}, {q_i8, "q_i8"}, {q_scale, "q_scale"}});
+  if (s == SAGE_OK) s = check_out(out);
   if (s != SAGE_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   return with_pool_workspace(ws_layout(B, S, S, H).total, st, [&](void* ws) {

@@ -94,6 +94,12 @@ def test_null_and_misaligned_pointers(lib):
     assert b"q is NULL" in lib.sage_last_error()
     assert _fwd(lib, v=FAKE + 8) == MISALIGNED
     assert b"v is not 16-byte aligned" in lib.sage_last_error()
+    # the attention kernel writes output rows as 32-byte vectors
+    assert _fwd(lib, out=FAKE + 16) == MISALIGNED
+    assert b"out is not 32-byte aligned" in lib.sage_last_error()
+    h = ctypes.c_void_p(0)
+    assert lib.sage_plan_create(P(FAKE), P(FAKE), P(FAKE), P(FAKE + 16), None, 1, 256, 256, 2, 128, 0.1,
+                                ctypes.byref(h)) == MISALIGNED
 
 
 def test_workspace_checks(lib):
