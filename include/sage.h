@@ -307,7 +307,7 @@ sage_status sage_debug_staging_codes(const void* q, const void* k, int B, int S,
 /* Fault sites of sage_debug_inject_fault. */
 enum {
   SAGE_FAULT_NONE = 0,          /* disarm */
-  SAGE_FAULT_POOL_ALLOC = 1,    /* a workspace / scratch allocation from the library's pool */
+  SAGE_FAULT_POOL_ALLOC = 1,    /* a workspace / scratch allocation (the library's pool, or a plan's workspace) */
   SAGE_FAULT_QUANT_LAUNCH = 2,  /* the Q/K quantisation launch of the attention entry points */
   SAGE_FAULT_ATTN_LAUNCH = 3    /* the attention kernel launch */
 };

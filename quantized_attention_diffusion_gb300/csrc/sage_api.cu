@@ -534,6 +534,7 @@ sage_status sage_plan_create(const void* q, const void* k, const void* v, void* 
   if (s != SAGE_OK) {
     if (exec) cudaGraphExecDestroy(exec);
     cudaFree(ws);
+    (void)cudaGetLastError();   // a failed capture leaves no error for the next call
     return s;
   }
   *plan = p;
