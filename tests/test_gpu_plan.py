@@ -142,3 +142,23 @@ def test_plan_on_a_side_stream_and_after_close():
     plan.close()
     with pytest.raises(RuntimeError):
         plan.launch()
+
+
+def test_out_must_be_32_byte_aligned():
+    """The attention kernel writes output rows as 32-byte vectors: an `out`
+    that is only 16-byte aligned is rejected on the host, before any launch,
+    by the direct call and by plan creation alike."""
+    import quantized_attention_diffusion_gb300 as qad
+    q, k, v = [t.cuda() for t in make_qkv(1, 64, 2, seed=315)]
+    n = q.numel()
+    buf = torch.zeros(n + 8, dtype=torch.bfloat16, device="cuda")      # 8 bf16 = 16 bytes
+    out16 = buf[8:].view(q.shape)
+    assert out16.data_ptr() % 32 == 16
+    with pytest.raises(qad.SageError) as ei:
+        qad.attn_fwd(q, k, v, out=out16)
+    assert ei.value.status == 3 and "32-byte" in str(ei.value)
+    with pytest.raises(qad.SageError) as ei:
+        qad.Plan(q, k, v, out=out16)
+    assert ei.value.status == 3
+    torch.cuda.synchronize()
+    assert bool((buf == 0).all())                                         # nothing was written
