@@ -53,6 +53,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include "qk_codes.cuh"
 #include "sage_internal.cuh"
 #include "sm103_ptx.cuh"
 
@@ -220,6 +221,7 @@ __device__ __forceinline__ float quantize_q_rows(uint8_t* tile, int r, int bh, i
   for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
   const float sc = __fdiv_rn(amax, 127.0f);
   const float rcp = __frcp_rn(sc);
+  const bool fast_sc = sc >= 0x1p-125f && sc <= 0x1p125f;
   const int grow = tile_row0 + r;
   int8_t* dump = (q_dump != nullptr && grow < Sq_pad)
                      ? q_dump + (static_cast<size_t>(bh) * Sq_pad + grow) * kHeadDim : nullptr;
@@ -229,17 +231,27 @@ __device__ __forceinline__ float quantize_q_rows(uint8_t* tile, int r, int bh, i
     uint4* cp = reinterpret_cast<uint4*>(tile + hf * kQHalf + roff + ((c ^ (r & 7)) << 4));
     const uint4 ch = *cp;
     const uint32_t w[4] = {ch.x, ch.y, ch.z, ch.w};
-    uint32_t h2[4], b4[2] = {0u, 0u};
+    float xs[8], code[8];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      const int lo = q_code(__uint_as_float(w[e] << 16), sc, rcp);
-      const int hi = q_code(__uint_as_float(w[e] & 0xFFFF0000u), sc, rcp);
-      const __half2 hh = __halves2half2(__int2half_rn(lo), __int2half_rn(hi));
+      xs[2 * e] = __uint_as_float(w[e] << 16);
+      xs[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
+    }
+    codes8(xs, sc, rcp, fast_sc, code);   // integer-valued, |code| <= 127: exact in fp16
+    uint32_t h2[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const __half2 hh = __floats2half2_rn(code[2 * e], code[2 * e + 1]);
       h2[e] = *reinterpret_cast<const uint32_t*>(&hh);
-      b4[e >> 1] |= ((static_cast<uint32_t>(lo) & 0xFFu) | ((static_cast<uint32_t>(hi) & 0xFFu) << 8)) << (16 * (e & 1));
     }
     *cp = make_uint4(h2[0], h2[1], h2[2], h2[3]);
-    if (dump) *reinterpret_cast<uint2*>(dump + hf * 64 + c * 8) = make_uint2(b4[0], b4[1]);
+    if (dump) {
+      uint32_t b8[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) b8[e] = (__float_as_uint(code[e] + kRoundMagic) - 0x4B400000u) & 0xFFu;
+      *reinterpret_cast<uint2*>(dump + hf * 64 + c * 8) =
+          make_uint2(b8[0] | (b8[1] << 8) | (b8[2] << 16) | (b8[3] << 24), b8[4] | (b8[5] << 8) | (b8[6] << 16) | (b8[7] << 24));
+    }
   }
   const int blk = (tile_row0 + (r & ~31)) / kQKBlock;
   if (q_scale_dump != nullptr && (r & 31) == 0 && blk < nbq)

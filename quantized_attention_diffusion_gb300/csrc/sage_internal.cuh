@@ -94,22 +94,5 @@ cudaError_t launch_wait_timeout_probe(uint64_t timeout_ns, cudaStream_t stream);
 // ------------------------------------------------------ device helpers --
 // Shared by the quantisation and attention kernels.
 
-// INT8 code of x for block scale sc, bit-identical to clamp(rint(x / sc),
-// -127, 127) with x / sc rounded to nearest even in fp32.  While 1/sc is a
-// normal float (sc in [2^-125, 2^125]), y = x * fl(1/sc) is within
-// |x/sc| * 2^-23 <= 1.6e-5 of x/sc (|x/sc| <= 127) and fl(x/sc) within
-// 7.6e-6, so both round to the same integer unless y lies within 2^-15 of a
-// half-integer; only then, or for extreme scales, is the division done.
-__device__ __forceinline__ int q_code(float x, float sc, float rcp) {
-  if (sc == 0.0f) return 0;
-  float y;
-  if (sc >= 0x1p-125f && sc <= 0x1p125f) {
-    y = x * rcp;
-    if (fabsf(y - floorf(y) - 0.5f) < 0x1p-15f) y = __fdiv_rn(x, sc);
-  } else {
-    y = __fdiv_rn(x, sc);
-  }
-  return static_cast<int>(fminf(fmaxf(rintf(y), -127.0f), 127.0f));
-}
 
 }  // namespace sage
