@@ -7,7 +7,11 @@ kernel, through the C ABI (``sage_attn_fwd``).  The metric is the pages'
 attention throughput, TOPS = 4*B*H*S^2*D / step time.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
-                  [--impl ours|reference]
+                  [--impl ours|reference] [--graph] [--lse|--fused-q|--smooth-k]
+
+``--graph`` replays each step from a ``sage_plan`` (the call recorded once
+as a CUDA graph) instead of calling ``sage_attn_fwd``; the kernels and their
+output are the same, only the per-call host work goes.
 
 N > 1 runs N independent replicas, one process per GPU (the method has no
 exchange step in one call): under torchrun each rank is one replica; run
