@@ -237,9 +237,10 @@ __device__ __forceinline__ long long bf16_fixed40(uint32_t h) {
 __global__ void __launch_bounds__(256) k_sum_kernel(const uint16_t* __restrict__ k, int S, int H,
                                                     unsigned long long* __restrict__ sums) {
   __shared__ long long part[16][kHeadDim];
-  const int bh = blockIdx.y, b = bh / H, h = bh % H;
+  const int nslices = (S + kVRowsPerCta - 1) / kVRowsPerCta;   // 1-D grid: block = bh * nslices + slice
+  const int bh = static_cast<int>(blockIdx.x / nslices), b = bh / H, h = bh % H;
   const int t = threadIdx.x, c8 = (t & 15) * 8, r = t >> 4;
-  const int s0 = blockIdx.x * kVRowsPerCta;
+  const int s0 = static_cast<int>(blockIdx.x % nslices) * kVRowsPerCta;
   const int s1 = min(S, s0 + kVRowsPerCta);
   const size_t tok_stride = static_cast<size_t>(H) * kHeadDim;
   const uint16_t* src = k + (static_cast<size_t>(b) * S * H + h) * kHeadDim + c8;
@@ -281,7 +282,7 @@ __device__ __forceinline__ uint8_t e4m3_code_div(float x, float sv) {
 }
 
 // Encode one 128-token tile of one (batch, head) and write it transposed.
-// grid = (S_pad / 128, B*H), 256 threads.
+// grid = (S_pad / 128) * B*H blocks (block bh * (S_pad / 128) + tile), 256 threads.
 //   Load: warp w covers tile tokens 16w .. 16w+15; in load instruction i
 //   (0..7) lanes 0-15 read token 16w + i and lanes 16-31 token 16w + 8 + i,
 //   lane l channels 8(l%16) .. +7 (16 bytes): two whole 256-byte rows per
@@ -321,11 +322,13 @@ __global__ void __launch_bounds__(kVEncThreads, 4) v_encode_kernel(const uint16_
   __shared__ __align__(16) float s_sv[kHeadDim];
   __shared__ __align__(16) float s_nr[kHeadDim];
   __shared__ __align__(16) int s_out[kHeadDim];   // scale outside [2^-100, 2^125]
-  const int bh = blockIdx.y, b = bh / H, h = bh % H;
+  const int ntiles = S_pad / 128;          // 1-D grid: block = bh * ntiles + tile
+  const int bh = static_cast<int>(blockIdx.x / ntiles), b = bh / H, h = bh % H;
+  const int tile_idx = static_cast<int>(blockIdx.x % ntiles);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane & 15;                 // channels 8g .. 8g+7
   const int tg = 2 * warp + (lane >> 4);   // token group: tile tokens 8tg .. 8tg+7
-  const int s0 = blockIdx.x * 128 + 8 * tg;
+  const int s0 = tile_idx * 128 + 8 * tg;
   const size_t tok_stride = static_cast<size_t>(H) * kHeadDim;
   const uint16_t* src = v + (static_cast<size_t>(b) * S * H + h) * kHeadDim + 8 * g + static_cast<size_t>(s0) * tok_stride;
   uint4 raw[8];
@@ -338,7 +341,7 @@ __global__ void __launch_bounds__(kVEncThreads, 4) v_encode_kernel(const uint16_
     s_sv[c] = sv;
     s_nr[c] = -__frcp_rn(sv);
     s_out[c] = !(sv >= 0x1p-100f && sv <= 0x1p125f);
-    if (blockIdx.x == 0) v_scale[static_cast<size_t>(bh) * kHeadDim + c] = sv;
+    if (tile_idx == 0) v_scale[static_cast<size_t>(bh) * kHeadDim + c] = sv;
   }
   __syncthreads();
   float sv[8], nr[8];
@@ -404,7 +407,7 @@ __global__ void __launch_bounds__(kVEncThreads, 4) v_encode_kernel(const uint16_
     const int c = it * (kVEncThreads / 8) + (threadIdx.x >> 3);
     const int gc = (c >> 3) & 15;
     const uint4 x = *reinterpret_cast<const uint4*>(tile + c * 128 + ((m ^ (gc >> 1)) << 4));
-    *reinterpret_cast<uint4*>(vt + (static_cast<size_t>(bh) * kHeadDim + c) * S_pad + blockIdx.x * 128 + 16 * m) = x;
+    *reinterpret_cast<uint4*>(vt + (static_cast<size_t>(bh) * kHeadDim + c) * S_pad + tile_idx * 128 + 16 * m) = x;
   }
 }
 
@@ -458,7 +461,9 @@ cudaError_t launch_qkv_quantize(const QKQuantArgs<CodeT>& a, const uint16_t* v, 
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || v == nullptr) return e;
   const int S_pad = a.S_pad[1];
-  v_encode_kernel<<<dim3(S_pad / 128, a.BH), kVEncThreads, 0, stream>>>(v, a.S[1], a.H, S_pad, amax_bits, vt,
+  const uint64_t v_blocks = static_cast<uint64_t>(S_pad / 128) * static_cast<uint64_t>(a.BH);
+  if (v_blocks > 0x7FFFFFFFull) return cudaErrorInvalidConfiguration;
+  v_encode_kernel<<<static_cast<unsigned>(v_blocks), kVEncThreads, 0, stream>>>(v, a.S[1], a.H, S_pad, amax_bits, vt,
                                                                          v_scale);
   return cudaGetLastError();
 }
@@ -479,7 +484,9 @@ cudaError_t launch_k_channel_means(const uint16_t* k, int B, int S, int H, unsig
   const int BH = B * H;
   cudaError_t e = cudaMemsetAsync(sums, 0, static_cast<size_t>(BH) * kHeadDim * sizeof(unsigned long long), stream);
   if (e != cudaSuccess) return e;
-  k_sum_kernel<<<dim3((S + kVRowsPerCta - 1) / kVRowsPerCta, BH), 256, 0, stream>>>(k, S, H, sums);
+  const uint64_t k_blocks = static_cast<uint64_t>((S + kVRowsPerCta - 1) / kVRowsPerCta) * static_cast<uint64_t>(BH);
+  if (k_blocks > 0x7FFFFFFFull) return cudaErrorInvalidConfiguration;
+  k_sum_kernel<<<static_cast<unsigned>(k_blocks), 256, 0, stream>>>(k, S, H, sums);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int n = BH * kHeadDim;

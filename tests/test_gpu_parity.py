@@ -274,3 +274,30 @@ def test_repeated_calls_are_bit_identical():
     torch.cuda.synchronize()
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
     assert torch.equal(s1.view(torch.int16), s2.view(torch.int16))
+
+
+def test_more_heads_than_a_grid_y_dimension_holds():
+    """B*H = 65600 (above the 65535 limit of a grid's y dimension): the V
+    encoder and the K channel sums index (tile, head) through a 1-D grid.
+    Quantisation bit-exact (with and without K smoothing), and the output on
+    sampled rows of the first, a middle and the last heads against the oracle."""
+    import quantized_attention_diffusion_gb300 as qad
+    B, S, H = 1, 3, 65600
+    qkv, bits = gen(B, S, H, "normal", 109)
+    ref = oracle.quantize(*bits)
+    _assert_quant_equal(_quantize_gpu(qkv), ref)
+    q, k, v = [t.cuda() for t in qkv]
+    got_s = [t.cpu().numpy() for t in qad.quantize_qkv_smooth_k(q, k, v)]
+    kc, ks, km = oracle.quantize_k_smooth(bits[1])
+    for name, g, r in (("k_i8", got_s[2], kc), ("k_scale", got_s[3], ks), ("k_mean", got_s[6], km)):
+        eq = (g.view(np.uint32) == r.view(np.uint32)) if g.dtype == np.float32 else (g == r)
+        assert eq.all(), f"smooth-K {name}: {int((~eq).sum())} mismatches"
+    scale = default_scale()
+    out = qad.attn_fwd(q, k, v, scale)
+    torch.cuda.synchronize()
+    heads = [0, 1, 32767, 65535, 65536, H - 1]
+    rows = np.array([(0, h, i) for h in heads for i in range(S)], dtype=np.int32)
+    ref_bits, ties = oracle.attend_rows(ref, S, scale, rows, return_ties=True)
+    o = out.float().cpu().numpy()
+    got = o[rows[:, 0], rows[:, 2], rows[:, 1]]
+    assert_close_to_oracle(got, f32(ref_bits), ties, f"H={H}")

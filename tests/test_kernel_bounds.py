@@ -26,7 +26,8 @@ def check_range(lo, hi, size, what):
 
 
 def v_encode_accesses(B, S, H):
-    """v_encode_kernel: grid (S_pad / 128, B*H), 256 threads.  Follows every
+    """v_encode_kernel: a 1-D grid of (S_pad / 128) * B*H blocks, block
+    bh * (S_pad / 128) + x for tile x of head bh, 256 threads.  Follows every
     byte: load instruction i (0..7) of lane l in warp w reads token
     128 x + 8 tg + i (tg = 2w + l/16; only tokens < S) at channels
     8g .. 8g+7 (g = l % 16, 16 bytes); the register transposes give channel
@@ -42,45 +43,47 @@ def v_encode_accesses(B, S, H):
     each tile store instruction takes two bank wavefronts."""
     Sp, BH = padded(S), B * H
     assert Sp % 128 == 0
+    ntiles = Sp // 128
     written = np.full(BH * D * Sp, -1, dtype=np.int64)        # V^T byte -> (token * D + channel)
-    for bh in range(BH):
+    blocks = [(idx // ntiles, idx % ntiles) for idx in range(ntiles * BH)]   # 1-D grid: bh * ntiles + tile
+    assert sorted(blocks) == [(bh, x) for bh in range(BH) for x in range(ntiles)]
+    for bh, x in blocks:
         b, h = bh // H, bh % H
-        for x in range(Sp // 128):
-            tile = np.full(D * 128, -1, dtype=np.int64)
-            for t in range(256):
-                lane, warp = t & 31, t >> 5
-                g, tg = lane & 15, 2 * warp + (lane >> 4)
+        tile = np.full(D * 128, -1, dtype=np.int64)
+        for t in range(256):
+            lane, warp = t & 31, t >> 5
+            g, tg = lane & 15, 2 * warp + (lane >> 4)
+            for i in range(8):
+                s = 128 * x + 8 * tg + i
+                if s < S:
+                    elem = ((b * S + s) * H + h) * D + 8 * g
+                    assert elem % 8 == 0 and 0 <= elem and elem + 8 <= B * S * H * D
+            mine = set()
+            for c in range(8):
+                addr = (8 * g + c) * 128 + ((tg ^ (g & 14)) << 3)
+                assert addr % 8 == 0 and 0 <= addr and addr + 8 <= D * 128
+                for j in range(8):
+                    assert tile[addr + j] == -1, "tile byte written twice"
+                    tile[addr + j] = (128 * x + 8 * tg + j) * D + 8 * g + c
+                    mine.add(addr + j)
+            chunk = 8 * g * 128 + ((tg ^ (g & 14)) << 3)
+            for c in range(8):
                 for i in range(8):
-                    s = 128 * x + 8 * tg + i
-                    if s < S:
-                        elem = ((b * S + s) * H + h) * D + 8 * g
-                        assert elem % 8 == 0 and 0 <= elem and elem + 8 <= B * S * H * D
-                mine = set()
-                for c in range(8):
-                    addr = (8 * g + c) * 128 + ((tg ^ (g & 14)) << 3)
-                    assert addr % 8 == 0 and 0 <= addr and addr + 8 <= D * 128
-                    for j in range(8):
-                        assert tile[addr + j] == -1, "tile byte written twice"
-                        tile[addr + j] = (128 * x + 8 * tg + j) * D + 8 * g + c
-                        mine.add(addr + j)
-                chunk = 8 * g * 128 + ((tg ^ (g & 14)) << 3)
-                for c in range(8):
-                    for i in range(8):
-                        assert chunk + c * 128 + i in mine          # division rewrite of its own byte
-                        assert tile[chunk + c * 128 + i] == (128 * x + 8 * tg + i) * D + 8 * g + c
-            assert np.all(tile >= 0)
-            for t in range(256):
-                m = t & 7
-                for it in range(4):
-                    c = it * 32 + (t >> 3)
-                    gc = (c >> 3) & 15
-                    a = c * 128 + ((m ^ (gc >> 1)) << 4)
-                    assert a % 16 == 0 and a + 16 <= D * 128
-                    piece = tile[a:a + 16]
-                    dst = (bh * D + c) * Sp + 128 * x + 16 * m
-                    assert dst % 16 == 0 and dst + 16 <= BH * D * Sp
-                    assert np.all(written[dst:dst + 16] == -1), "V^T byte written twice"
-                    written[dst:dst + 16] = piece
+                    assert chunk + c * 128 + i in mine          # division rewrite of its own byte
+                    assert tile[chunk + c * 128 + i] == (128 * x + 8 * tg + i) * D + 8 * g + c
+        assert np.all(tile >= 0)
+        for t in range(256):
+            m = t & 7
+            for it in range(4):
+                c = it * 32 + (t >> 3)
+                gc = (c >> 3) & 15
+                a = c * 128 + ((m ^ (gc >> 1)) << 4)
+                assert a % 16 == 0 and a + 16 <= D * 128
+                piece = tile[a:a + 16]
+                dst = (bh * D + c) * Sp + 128 * x + 16 * m
+                assert dst % 16 == 0 and dst + 16 <= BH * D * Sp
+                assert np.all(written[dst:dst + 16] == -1), "V^T byte written twice"
+                written[dst:dst + 16] = piece
     tok = np.arange(Sp)[None, :]
     ch = np.arange(D)[:, None]
     expect = np.broadcast_to(tok * D + ch, (D, Sp))
