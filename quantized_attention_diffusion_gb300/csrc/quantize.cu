@@ -453,6 +453,7 @@ cudaError_t launch_qkv_quantize(const QKQuantArgs<CodeT>& a, const uint16_t* v, 
   const long long blocks = static_cast<long long>(a.BH) * (std::max(a.first ? 0 : a.S_pad[0], a.S_pad[1]) / 32);
   long long ctas = (blocks + 7) / 8;
   if (v != nullptr) ctas = std::max(ctas, static_cast<long long>(a.BH) * vm.nslices);
+  if (ctas > 0x7FFFFFFFll) return cudaErrorInvalidConfiguration;
   const dim3 grid(static_cast<unsigned>(ctas), (v != nullptr ? 3 : 2) - a.first);
   if (a.k_mean != nullptr)
     qkv_pass1_kernel<CodeT, true><<<grid, 256, 0, stream>>>(a, vm);
