@@ -158,6 +158,16 @@ __device__ __forceinline__ void qk_warp(const QKQuantArgs<CodeT>& a, int tensor)
 // must start at 0.
 constexpr int kVRowsPerCta = 256;
 
+// Grids over (x blocks per head, heads): the head index spans y and z, y
+// below 65535 (the y and z limit), so B*H up to 2^31 - 1 fits; x runs
+// fastest, so a head's blocks are adjacent in launch order.
+constexpr unsigned kGridYMax = 65535;
+inline dim3 heads_grid(int x, int heads) {
+  const unsigned y = static_cast<unsigned>(heads < static_cast<int>(kGridYMax) ? heads : static_cast<int>(kGridYMax));
+  const unsigned z = (static_cast<unsigned>(heads) + kGridYMax - 1) / kGridYMax;
+  return dim3(static_cast<unsigned>(x), y, z);
+}
+
 __device__ __forceinline__ void v_amax_slice(const uint16_t* __restrict__ v, int S, int H,
                                              uint32_t* __restrict__ amax_bits, int bh, int slice) {
   __shared__ float part[16][kHeadDim];
@@ -234,13 +244,15 @@ __device__ __forceinline__ long long bf16_fixed40(uint32_t h) {
 // 64-bit fixed point (2^-40): integer additions, so the merged result does not
 // depend on the order of the slices, and it equals the exact sum for the
 // magnitudes bf16_fixed40 keeps exactly.
-__global__ void __launch_bounds__(256) k_sum_kernel(const uint16_t* __restrict__ k, int S, int H,
+__global__ void __launch_bounds__(256) k_sum_kernel(const uint16_t* __restrict__ k, int S, int H, int BH,
                                                     unsigned long long* __restrict__ sums) {
   __shared__ long long part[16][kHeadDim];
-  const int nslices = (S + kVRowsPerCta - 1) / kVRowsPerCta;   // 1-D grid: block = bh * nslices + slice
-  const int bh = static_cast<int>(blockIdx.x / nslices), b = bh / H, h = bh % H;
+  // grid (slices, heads): the head index spans y and z (y < 65535).
+  const int bh = static_cast<int>(blockIdx.z * kGridYMax + blockIdx.y);
+  if (bh >= BH) return;                    // CTA-uniform, before any barrier
+  const int b = bh / H, h = bh % H;
   const int t = threadIdx.x, c8 = (t & 15) * 8, r = t >> 4;
-  const int s0 = static_cast<int>(blockIdx.x % nslices) * kVRowsPerCta;
+  const int s0 = static_cast<int>(blockIdx.x) * kVRowsPerCta;
   const int s1 = min(S, s0 + kVRowsPerCta);
   const size_t tok_stride = static_cast<size_t>(H) * kHeadDim;
   const uint16_t* src = k + (static_cast<size_t>(b) * S * H + h) * kHeadDim + c8;
@@ -282,7 +294,7 @@ __device__ __forceinline__ uint8_t e4m3_code_div(float x, float sv) {
 }
 
 // Encode one 128-token tile of one (batch, head) and write it transposed.
-// grid = (S_pad / 128) * B*H blocks (block bh * (S_pad / 128) + tile), 256 threads.
+// grid = (S_pad / 128, heads) through heads_grid, 256 threads.
 //   Load: warp w covers tile tokens 16w .. 16w+15; in load instruction i
 //   (0..7) lanes 0-15 read token 16w + i and lanes 16-31 token 16w + 8 + i,
 //   lane l channels 8(l%16) .. +7 (16 bytes): two whole 256-byte rows per
@@ -314,7 +326,7 @@ __device__ __forceinline__ uint8_t e4m3_code_div(float x, float sv) {
 constexpr int kVEncThreads = 256;
 
 __global__ void __launch_bounds__(kVEncThreads, 4) v_encode_kernel(const uint16_t* __restrict__ v, int S, int H,
-                                                                   int S_pad,
+                                                                   int BH, int S_pad,
                                                                    const uint32_t* __restrict__ amax_bits,
                                                                    uint8_t* __restrict__ vt,
                                                                    float* __restrict__ v_scale) {
@@ -322,9 +334,11 @@ __global__ void __launch_bounds__(kVEncThreads, 4) v_encode_kernel(const uint16_
   __shared__ __align__(16) float s_sv[kHeadDim];
   __shared__ __align__(16) float s_nr[kHeadDim];
   __shared__ __align__(16) int s_out[kHeadDim];   // scale outside [2^-100, 2^125]
-  const int ntiles = S_pad / 128;          // 1-D grid: block = bh * ntiles + tile
-  const int bh = static_cast<int>(blockIdx.x / ntiles), b = bh / H, h = bh % H;
-  const int tile_idx = static_cast<int>(blockIdx.x % ntiles);
+  // grid (tiles, heads): the head index spans y and z (y < 65535).
+  const int bh = static_cast<int>(blockIdx.z * kGridYMax + blockIdx.y);
+  if (bh >= BH) return;                    // CTA-uniform, before any barrier
+  const int b = bh / H, h = bh % H;
+  const int tile_idx = static_cast<int>(blockIdx.x);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane & 15;                 // channels 8g .. 8g+7
   const int tg = 2 * warp + (lane >> 4);   // token group: tile tokens 8tg .. 8tg+7
@@ -462,9 +476,7 @@ cudaError_t launch_qkv_quantize(const QKQuantArgs<CodeT>& a, const uint16_t* v, 
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || v == nullptr) return e;
   const int S_pad = a.S_pad[1];
-  const uint64_t v_blocks = static_cast<uint64_t>(S_pad / 128) * static_cast<uint64_t>(a.BH);
-  if (v_blocks > 0x7FFFFFFFull) return cudaErrorInvalidConfiguration;
-  v_encode_kernel<<<static_cast<unsigned>(v_blocks), kVEncThreads, 0, stream>>>(v, a.S[1], a.H, S_pad, amax_bits, vt,
+  v_encode_kernel<<<heads_grid(S_pad / 128, a.BH), kVEncThreads, 0, stream>>>(v, a.S[1], a.H, a.BH, S_pad, amax_bits, vt,
                                                                          v_scale);
   return cudaGetLastError();
 }
@@ -485,9 +497,7 @@ cudaError_t launch_k_channel_means(const uint16_t* k, int B, int S, int H, unsig
   const int BH = B * H;
   cudaError_t e = cudaMemsetAsync(sums, 0, static_cast<size_t>(BH) * kHeadDim * sizeof(unsigned long long), stream);
   if (e != cudaSuccess) return e;
-  const uint64_t k_blocks = static_cast<uint64_t>((S + kVRowsPerCta - 1) / kVRowsPerCta) * static_cast<uint64_t>(BH);
-  if (k_blocks > 0x7FFFFFFFull) return cudaErrorInvalidConfiguration;
-  k_sum_kernel<<<static_cast<unsigned>(k_blocks), 256, 0, stream>>>(k, S, H, sums);
+  k_sum_kernel<<<heads_grid((S + kVRowsPerCta - 1) / kVRowsPerCta, BH), 256, 0, stream>>>(k, S, H, BH, sums);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int n = BH * kHeadDim;

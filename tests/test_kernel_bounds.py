@@ -25,9 +25,37 @@ def check_range(lo, hi, size, what):
     assert np.all(hi <= size), (what, int(hi.max()), size)
 
 
+GRID_Y_MAX = 65535
+
+
+def heads_grid_blocks(x_blocks, heads):
+    """(bh, x) of every live block of a grid from heads_grid(x_blocks,
+    heads): dim3(x, min(heads, 65535), ceil(heads / 65535)), head index
+    z * 65535 + y, blocks with bh >= heads returning at once."""
+    gy, gz = min(heads, GRID_Y_MAX), (heads + GRID_Y_MAX - 1) // GRID_Y_MAX
+    assert gy <= 65535 and gz <= 65535
+    out = []
+    for z in range(gz):
+        for y in range(gy):
+            bh = z * GRID_Y_MAX + y
+            if bh < heads:
+                out.extend((bh, x) for x in range(x_blocks))
+    return out
+
+
+def test_heads_grid_covers_every_head_once():
+    for heads in (1, 2, 65534, 65535, 65536, 65600, 131071, 200000):
+        gy, gz = min(heads, GRID_Y_MAX), (heads + GRID_Y_MAX - 1) // GRID_Y_MAX
+        bhs = np.add.outer(np.arange(gz) * GRID_Y_MAX, np.arange(gy)).ravel()
+        live = bhs[bhs < heads]
+        assert np.array_equal(np.sort(live), np.arange(heads)), heads
+    # the largest B*H the ABI takes still fits the y and z limits
+    assert (2 ** 31 - 1 + GRID_Y_MAX - 1) // GRID_Y_MAX <= 65535
+
+
 def v_encode_accesses(B, S, H):
-    """v_encode_kernel: a 1-D grid of (S_pad / 128) * B*H blocks, block
-    bh * (S_pad / 128) + x for tile x of head bh, 256 threads.  Follows every
+    """v_encode_kernel: grid (S_pad / 128, heads) as heads_grid forms it,
+    block (x, y, z) for tile x of head bh = z * 65535 + y, 256 threads.  Follows every
     byte: load instruction i (0..7) of lane l in warp w reads token
     128 x + 8 tg + i (tg = 2w + l/16; only tokens < S) at channels
     8g .. 8g+7 (g = l % 16, 16 bytes); the register transposes give channel
@@ -45,8 +73,7 @@ def v_encode_accesses(B, S, H):
     assert Sp % 128 == 0
     ntiles = Sp // 128
     written = np.full(BH * D * Sp, -1, dtype=np.int64)        # V^T byte -> (token * D + channel)
-    blocks = [(idx // ntiles, idx % ntiles) for idx in range(ntiles * BH)]   # 1-D grid: bh * ntiles + tile
-    assert sorted(blocks) == [(bh, x) for bh in range(BH) for x in range(ntiles)]
+    blocks = heads_grid_blocks(ntiles, BH)
     for bh, x in blocks:
         b, h = bh // H, bh % H
         tile = np.full(D * 128, -1, dtype=np.int64)
