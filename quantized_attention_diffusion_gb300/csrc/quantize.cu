@@ -216,6 +216,10 @@ struct VMaxArgs {
 
 template <typename CodeT, bool kSmooth>
 __global__ void __launch_bounds__(256, 2) qkv_pass1_kernel(QKQuantArgs<CodeT> a, VMaxArgs vm) {
+  // The V^T encoder launched after this grid may be scheduled once every CTA
+  // here has started (it waits for this grid's completion before reading the
+  // channel maxima), so its V loads overlap this grid's last wave.
+  asm volatile("griddepcontrol.launch_dependents;");
   const int role = blockIdx.y + a.first;
   if (role == 2) {
     const long long idx = blockIdx.x;
@@ -351,6 +355,9 @@ __global__ void __launch_bounds__(kVEncThreads, 4) v_encode_kernel(const uint16_
     raw[i] = s0 + i < S ? __ldcs(reinterpret_cast<const uint4*>(src + i * tok_stride)) : make_uint4(0, 0, 0, 0);
   if (threadIdx.x < kHeadDim) {
     const int c = threadIdx.x;
+    // The channel maxima come from the preceding grid: wait for its
+    // completion (a no-op when this grid was not launched as its dependent).
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const float sv = __fdiv_rn(__uint_as_float(amax_bits[static_cast<size_t>(bh) * kHeadDim + c]), 448.0f);
     s_sv[c] = sv;
     s_nr[c] = -__frcp_rn(sv);
@@ -476,9 +483,19 @@ cudaError_t launch_qkv_quantize(const QKQuantArgs<CodeT>& a, const uint16_t* v, 
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || v == nullptr) return e;
   const int S_pad = a.S_pad[1];
-  v_encode_kernel<<<heads_grid(S_pad / 128, a.BH), kVEncThreads, 0, stream>>>(v, a.S[1], a.H, a.BH, S_pad, amax_bits, vt,
-                                                                         v_scale);
-  return cudaGetLastError();
+  // Launched as a programmatic dependent of the first pass (see the kernels).
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = heads_grid(S_pad / 128, a.BH);
+  cfg.blockDim = dim3(kVEncThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, v_encode_kernel, v, a.S[1], a.H, a.BH, S_pad,
+                            static_cast<const uint32_t*>(amax_bits), vt, v_scale);
 }
 cudaError_t load_quantize_kernels() {
   cudaFuncAttributes fa;
