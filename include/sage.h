@@ -63,9 +63,10 @@ int64_t sage_padded_len(int S);
 
 /* Number of kernels one call of sage_attn_fwd, _ws, _lse, _cross or _fused_q
  * launches for this shape (Sq = Skv for self-attention), or of
- * sage_attn_fwd_smooth_k when smooth_k is non-zero: Q/K quantisation, V
- * maxima, V encoding, attention (and for smooth_k the K channel sums and
- * means).  Returns -1 for an invalid shape.  No device work. */
+ * sage_attn_fwd_smooth_k when smooth_k is non-zero: zeroing of the V maxima,
+ * Q/K quantisation with the V maxima, V encoding, attention (and for
+ * smooth_k the K channel sums and means).  Returns -1 for an invalid shape.
+ * No device work. */
 int sage_attn_fwd_launches(int B, int Sq, int Skv, int H, int smooth_k);
 
 /* Bytes of device workspace sage_attn_fwd_ws() / sage_attn_fwd_quantized()

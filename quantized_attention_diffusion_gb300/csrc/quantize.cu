@@ -162,6 +162,35 @@ constexpr int kVRowsPerCta = 256;
 // below 65535 (the y and z limit), so B*H up to 2^31 - 1 fits; x runs
 // fastest, so a head's blocks are adjacent in launch order.
 constexpr unsigned kGridYMax = 65535;
+
+// Zeroes n words (the channel maxima the first pass merges with atomicMax).
+// Its dependent, the first pass, may start at once: only that pass's V
+// maxima role waits for this grid before touching these words.
+__global__ void __launch_bounds__(256) zero_words_kernel(uint32_t* __restrict__ p, size_t n) {
+  asm volatile("griddepcontrol.launch_dependents;");
+  const size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i < n) p[i] = 0u;
+}
+
+// Launch `kernel` as a programmatic dependent of the grid before it on
+// `stream` (programmatic stream serialisation): it may be scheduled once
+// every CTA of that grid has triggered or finished, and must itself wait
+// (griddepcontrol.wait) before reading anything that grid writes.
+template <typename... Params, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(Params...), dim3 grid, dim3 block, cudaStream_t stream,
+                             Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Params>(args)...);
+}
 inline dim3 heads_grid(int x, int heads) {
   const unsigned y = static_cast<unsigned>(heads < static_cast<int>(kGridYMax) ? heads : static_cast<int>(kGridYMax));
   const unsigned z = (static_cast<unsigned>(heads) + kGridYMax - 1) / kGridYMax;
@@ -198,6 +227,9 @@ __device__ __forceinline__ void v_amax_slice(const uint16_t* __restrict__ v, int
   for (int i = 0; i < 8; ++i) part[r][c8 + i] = m[i];
   __syncthreads();
   if (t < kHeadDim) {
+    // The words were zeroed by the grid before this one, which this grid may
+    // have started ahead of.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     float mm = part[0][t];
 #pragma unroll
     for (int i = 1; i < 16; ++i) mm = fmaxf(mm, part[i][t]);
@@ -468,7 +500,9 @@ cudaError_t launch_qkv_quantize(const QKQuantArgs<CodeT>& a, const uint16_t* v, 
   vm.BH = a.BH;
   vm.nslices = (a.S[1] + kVRowsPerCta - 1) / kVRowsPerCta;
   if (v != nullptr) {
-    cudaError_t e = cudaMemsetAsync(amax_bits, 0, static_cast<size_t>(a.BH) * kHeadDim * sizeof(uint32_t), stream);
+    const size_t n = static_cast<size_t>(a.BH) * kHeadDim;
+    zero_words_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, stream>>>(amax_bits, n);
+    cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
   const long long blocks = static_cast<long long>(a.BH) * (std::max(a.first ? 0 : a.S_pad[0], a.S_pad[1]) / 32);
@@ -476,26 +510,25 @@ cudaError_t launch_qkv_quantize(const QKQuantArgs<CodeT>& a, const uint16_t* v, 
   if (v != nullptr) ctas = std::max(ctas, static_cast<long long>(a.BH) * vm.nslices);
   if (ctas > 0x7FFFFFFFll) return cudaErrorInvalidConfiguration;
   const dim3 grid(static_cast<unsigned>(ctas), (v != nullptr ? 3 : 2) - a.first);
-  if (a.k_mean != nullptr)
-    qkv_pass1_kernel<CodeT, true><<<grid, 256, 0, stream>>>(a, vm);
-  else
-    qkv_pass1_kernel<CodeT, false><<<grid, 256, 0, stream>>>(a, vm);
-  cudaError_t e = cudaGetLastError();
+  // With V, the first pass is a programmatic dependent of the zeroing kernel
+  // just launched (its Q/K roles never read what that kernel writes);
+  // without V nothing precedes it that it may overlap.
+  cudaError_t e;
+  if (v != nullptr) {
+    e = a.k_mean != nullptr ? launch_dependent(qkv_pass1_kernel<CodeT, true>, grid, dim3(256), stream, a, vm)
+                            : launch_dependent(qkv_pass1_kernel<CodeT, false>, grid, dim3(256), stream, a, vm);
+  } else {
+    if (a.k_mean != nullptr)
+      qkv_pass1_kernel<CodeT, true><<<grid, 256, 0, stream>>>(a, vm);
+    else
+      qkv_pass1_kernel<CodeT, false><<<grid, 256, 0, stream>>>(a, vm);
+    e = cudaGetLastError();
+  }
   if (e != cudaSuccess || v == nullptr) return e;
   const int S_pad = a.S_pad[1];
-  // Launched as a programmatic dependent of the first pass (see the kernels).
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = heads_grid(S_pad / 128, a.BH);
-  cfg.blockDim = dim3(kVEncThreads);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, v_encode_kernel, v, a.S[1], a.H, a.BH, S_pad,
-                            static_cast<const uint32_t*>(amax_bits), vt, v_scale);
+  // A programmatic dependent of the first pass (see the kernels).
+  return launch_dependent(v_encode_kernel, heads_grid(S_pad / 128, a.BH), dim3(kVEncThreads), stream, v, a.S[1],
+                          a.H, a.BH, S_pad, static_cast<const uint32_t*>(amax_bits), vt, v_scale);
 }
 cudaError_t load_quantize_kernels() {
   cudaFuncAttributes fa;

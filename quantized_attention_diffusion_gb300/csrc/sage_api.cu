@@ -347,9 +347,9 @@ int64_t sage_padded_len(int S) { return S < 1 ? 0 : static_cast<int64_t>(padded_
 
 int sage_attn_fwd_launches(int B, int Sq, int Skv, int H, int smooth_k) {
   if (B < 1 || Sq < 1 || Skv < 1 || H < 1) return -1;
-  // Q/K quantisation with the V maxima, V encoding, attention; K smoothing
-  // adds the channel sums and means.
-  return 3 + (smooth_k ? 2 : 0);
+  // Zeroing of the V maxima, Q/K quantisation with the V maxima, V encoding,
+  // attention; K smoothing adds the channel sums and means.
+  return 4 + (smooth_k ? 2 : 0);
 }
 
 size_t sage_workspace_bytes(int B, int S, int H, int D) {

@@ -51,13 +51,13 @@ def test_no_cuda_runtime_dependency_on_host_checks(lib):
 
 
 def test_launch_count(lib):
-    assert lib.sage_attn_fwd_launches(2, 16384, 16384, 24, 0) == 3
-    assert lib.sage_attn_fwd_launches(2, 16384, 16384, 24, 1) == 5
-    assert lib.sage_attn_fwd_launches(2, 16384, 333, 24, 0) == 3
+    assert lib.sage_attn_fwd_launches(2, 16384, 16384, 24, 0) == 4
+    assert lib.sage_attn_fwd_launches(2, 16384, 16384, 24, 1) == 6
+    assert lib.sage_attn_fwd_launches(2, 16384, 333, 24, 0) == 4
     assert lib.sage_attn_fwd_launches(0, 16, 16, 1, 0) == -1
     assert lib.sage_attn_fwd_launches(1, 16, 0, 1, 0) == -1
-    assert qad.attn_fwd_launches(2, 16384, 24) == 3
-    assert qad.attn_fwd_launches(2, 16384, 24, smooth_k=True) == 5
+    assert qad.attn_fwd_launches(2, 16384, 24) == 4
+    assert qad.attn_fwd_launches(2, 16384, 24, smooth_k=True) == 6
 
 
 def test_workspace_bytes(lib):
