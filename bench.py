@@ -281,6 +281,11 @@ def tensor_peak():
 # N=256, K=16 in 128 clocks), E4M3 twice that; GB300 has 152 SMs.
 FP16_FLOP_PER_CLK_SM = 8192
 N_SMS = 152
+# ex2.approx results per clock per SM: one warp instruction per 4 clocks per
+# sub-partition (the attention kernel's XU counter matches its ex2 count at
+# that rate); the softmax takes one per score element.
+EX2_PER_CLK_SM = 32
+MAX_SM_MHZ = 2070
 
 
 def attention_traffic():
@@ -485,6 +490,8 @@ def run_ours(args, group, local):
     clock_peak = None
     if clocks.get("sm_mhz"):
         clock_peak = 4.0 / 3.0 * FP16_FLOP_PER_CLK_SM * N_SMS * clocks["sm_mhz"] * 1e6 / 1e12
+    exps = w.B * w.H * w.S * w.skv
+    xu_ms = exps / (EX2_PER_CLK_SM * N_SMS * (clocks.get("sm_mhz") or MAX_SM_MHZ) * 1e6) * 1e3
     line = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -524,6 +531,10 @@ def run_ours(args, group, local):
             "peak_sustained": round(peak_sust, 1), "frac_vs_sustained": round(achieved / peak_sust, 4),
             "peak_at_sampled_clock": round(clock_peak, 1) if clock_peak else None,
             "frac_vs_sampled_clock": round(achieved / clock_peak, 4) if clock_peak else None,
+            "secondary": {"xu": {"exp2_per_launch": exps, "floor_ms": round(xu_ms, 4),
+                                 "frac": round(xu_ms / attn_ms_max, 4),
+                                 "basis": f"one ex2.approx per score element, {N_SMS} SMs x {EX2_PER_CLK_SM} "
+                                          f"per clock at the sampled SM clock"}},
         },
         "clocks": clocks,
     }
