@@ -10,7 +10,8 @@ attention throughput, TOPS = 4*B*H*S^2*D / step time.
                   [--impl ours|reference] [--graph] [--lse|--fused-q|--smooth-k]
 
 ``--graph`` replays each step from a ``sage_plan`` (the call recorded once
-as a CUDA graph) instead of calling ``sage_attn_fwd``; the kernels and their
+as a CUDA graph, with ``--fused-q`` or ``--smooth-k`` that variant) instead
+of calling ``sage_attn_fwd``; the kernels and their
 output are the same, only the per-call host work goes.
 
 N > 1 runs N independent replicas, one process per GPU (the method has no
@@ -367,14 +368,15 @@ def run_ours(args, group, local):
         else:
             qad.attn_fwd(qq, kk, vv, w.softmax_scale, out=oo, fused_q=args.fused_q, smooth_k=args.smooth_k)
 
-    if args.graph and (args.fused_q or args.smooth_k):
-        raise SystemExit("--graph records sage_attn_fwd / _lse / _cross calls only")
+    if args.lse + args.fused_q + args.smooth_k > 1 or ((args.fused_q or args.smooth_k) and w.Skv is not None):
+        raise SystemExit("--lse, --fused-q and --smooth-k select one call each; the last two are self-attention")
     plans = {}
 
     def plan_step(qq, kk, vv, oo, ll=None):
         key = (qq.data_ptr(), oo.data_ptr())
         if key not in plans:                                 # recorded once per buffer set, before timing
-            plans[key] = qad.Plan(qq, kk, vv, w.softmax_scale, out=oo, lse=ll)
+            plans[key] = qad.Plan(qq, kk, vv, w.softmax_scale, out=oo, lse=ll, smooth_k=args.smooth_k,
+                                  fused_q=args.fused_q)
         plans[key].launch()
 
     run = plan_step if args.graph else step

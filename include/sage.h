@@ -44,7 +44,7 @@ extern "C" {
 typedef enum sage_status {
   SAGE_OK = 0,
   SAGE_ERR_INVALID_ARG = 1, /* a size < 1, a NULL pointer, a non-finite or non-positive scale */
-  SAGE_ERR_UNSUPPORTED = 2, /* head dimension other than 128 */
+  SAGE_ERR_UNSUPPORTED = 2, /* head dimension other than 128; a plan option not offered */
   SAGE_ERR_MISALIGNED = 3,  /* a pointer not 16-byte aligned (an attention `out` not 32-byte aligned) */
   SAGE_ERR_CUDA = 4,        /* a CUDA runtime or launch error (message kept) */
   SAGE_ERR_NO_MEMORY = 5,   /* workspace allocation failed */
@@ -210,10 +210,22 @@ sage_status sage_attn_fwd_cross(const void* q, const void* k, const void* v, voi
  *   nothing.  Errors: INVALID_ARG (plan NULL, other device), CUDA.
  * sage_plan_destroy: frees the plan and its workspace (cudaFree, which waits
  *   for the device's outstanding work).  NULL is a no-op.  Errors: CUDA.
+ * sage_plan_create_ex: sage_plan_create recording one of the variant calls
+ *   instead, chosen by `flags`: SAGE_PLAN_SMOOTH_K records
+ *   sage_attn_fwd_smooth_k (K smoothing before the attention step),
+ *   SAGE_PLAN_FUSED_Q records sage_attn_fwd_fused_q (Q quantised inside the
+ *   attention kernel); 0 is sage_plan_create.  The results are those calls'
+ *   (bit for bit).  Both variants are self-attention without LSE, so a flag
+ *   needs Sq == Skv and lse NULL (INVALID_ARG otherwise); both flags at once
+ *   or an unknown bit: UNSUPPORTED.  Everything else as sage_plan_create.
  */
 typedef struct sage_plan sage_plan;
+#define SAGE_PLAN_SMOOTH_K 1u
+#define SAGE_PLAN_FUSED_Q 2u
 sage_status sage_plan_create(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Sq,
                              int Skv, int H, int D, float softmax_scale, sage_plan** plan);
+sage_status sage_plan_create_ex(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Sq,
+                                int Skv, int H, int D, float softmax_scale, unsigned flags, sage_plan** plan);
 sage_status sage_plan_launch(sage_plan* plan, void* stream);
 sage_status sage_plan_destroy(sage_plan* plan);
 

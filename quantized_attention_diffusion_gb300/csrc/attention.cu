@@ -136,16 +136,6 @@ __device__ __forceinline__ void drain_bar(uint64_t* bar, uint32_t parity, uint64
   (void)mbar_wait(bar, parity, &local_abort, &g_sage_error, timeout_ns);
 }
 
-__device__ __forceinline__ void store_bf16x8(uint16_t* dst, const float (&v)[8]) {
-  uint32_t w[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    __nv_bfloat162 b = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
-    w[i] = *reinterpret_cast<uint32_t*>(&b);
-  }
-  *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
-}
-
 // Sixteen floats -> sixteen bf16 (round to nearest even) in one 32-byte
 // store; dst must be 32-byte aligned.
 __device__ __forceinline__ void store_bf16x16(uint16_t* dst, const float (&v)[16]) {

@@ -474,8 +474,20 @@ sage_status sage_attn_fwd_cross(const void* q, const void* k, const void* v, voi
 
 sage_status sage_plan_create(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Sq,
                              int Skv, int H, int D, float softmax_scale, sage_plan** plan) {
+  return sage_plan_create_ex(q, k, v, out, lse, B, Sq, Skv, H, D, softmax_scale, 0u, plan);
+}
+
+sage_status sage_plan_create_ex(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Sq,
+                                int Skv, int H, int D, float softmax_scale, unsigned flags, sage_plan** plan) {
   if (!plan) return fail(SAGE_ERR_INVALID_ARG, "plan is NULL");
   *plan = nullptr;
+  if ((flags & ~(SAGE_PLAN_SMOOTH_K | SAGE_PLAN_FUSED_Q)) != 0u ||
+      flags == (SAGE_PLAN_SMOOTH_K | SAGE_PLAN_FUSED_Q))
+    return fail(SAGE_ERR_UNSUPPORTED, "plan flags 0x%x: no call offers that combination", flags);
+  const bool smooth_k = (flags & SAGE_PLAN_SMOOTH_K) != 0u, fuse_q = (flags & SAGE_PLAN_FUSED_Q) != 0u;
+  if (flags != 0u && (Sq != Skv || lse != nullptr))
+    return fail(SAGE_ERR_INVALID_ARG, "plan flags 0x%x record a self-attention call without LSE (Sq %d, Skv %d%s)",
+                flags, Sq, Skv, lse ? ", lse given" : "");
   sage_status s = check_shape(B, Sq, H, D);
   if (s == SAGE_OK) s = check_shape(B, Skv, H, D);
   if (s == SAGE_OK) s = check_scale(softmax_scale);
@@ -512,7 +524,7 @@ sage_status sage_plan_create(const void* q, const void* k, const void* v, void* 
   t_attn_before = t_attn_after = nullptr;
   e = cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal);
   if (e == cudaSuccess) {
-    s = run_fused(q, k, v, out, B, Sq, Skv, H, softmax_scale, ws, cs, lse);
+    s = run_fused(q, k, v, out, B, Sq, Skv, H, softmax_scale, ws, cs, lse, fuse_q, nullptr, nullptr, smooth_k);
     const cudaError_t e_end = cudaStreamEndCapture(cs, &graph);   // ends the capture whatever happened
     if (s == SAGE_OK && e_end != cudaSuccess) s = cuda_fail(e_end, "plan capture");
   } else {

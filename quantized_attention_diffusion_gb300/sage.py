@@ -37,8 +37,11 @@ EXPORTED = (
     "sage_debug_fused_q", "sage_attn_fwd_fused_q", "sage_quantize_qkv_smooth_k",
     "sage_attn_fwd_smooth_k", "sage_attn_fwd_launches", "sage_debug_staging_codes",
     "sage_debug_inject_fault", "sage_debug_pool_state", "sage_plan_create", "sage_plan_launch",
-    "sage_plan_destroy",
+    "sage_plan_destroy", "sage_plan_create_ex",
 )
+
+# Options of sage_plan_create_ex (include/sage.h).
+PLAN_SMOOTH_K, PLAN_FUSED_Q = 1, 2
 
 # Fault sites of sage_debug_inject_fault (include/sage.h).
 FAULT_NONE, FAULT_POOL_ALLOC, FAULT_QUANT_LAUNCH, FAULT_ATTN_LAUNCH = 0, 1, 2, 3
@@ -80,6 +83,7 @@ def load_library(path: str = LIB_PATH):
             "sage_attn_fwd_lse": (S, [P, P, P, P, P, I, I, I, I, F, P]),
             "sage_attn_fwd_cross": (S, [P, P, P, P, P, I, I, I, I, I, F, P]),
             "sage_plan_create": (S, [P, P, P, P, P, I, I, I, I, I, F, P]),
+            "sage_plan_create_ex": (S, [P, P, P, P, P, I, I, I, I, I, F, ctypes.c_uint, P]),
             "sage_plan_launch": (S, [P, P]),
             "sage_plan_destroy": (S, [P]),
             "sage_debug_fused_q": (S, [P, P, P, P, I, I, I, I, F, P, P, P]),
@@ -249,15 +253,18 @@ def attn_fwd_cross(q, k, v, softmax_scale: float | None = None, out=None, lse=No
 
 
 class Plan:
-    """One fixed attention call recorded as a CUDA graph (sage_plan_create):
+    """One fixed attention call recorded as a CUDA graph (sage_plan_create_ex):
     q bf16 [B, Sq, H, 128], k and v bf16 [B, Skv, H, 128] (Skv = Sq for
     self-attention), out bf16 [B, Sq, H, 128] and optionally lse fp32
-    [B, H, Sq], all fixed at creation.  ``launch()`` replays the call on the
-    current stream, reading q, k and v as they are then; launches of one plan
-    must not overlap (one stream, or ordered).  ``close()`` (or leaving a
-    ``with`` block) releases the graph and its workspace."""
+    [B, H, Sq], all fixed at creation.  ``smooth_k`` records attn_fwd_smooth_k
+    instead and ``fused_q`` attn_fwd_fused_q (self-attention without lse, one
+    at a time).  ``launch()`` replays the call on the current stream, reading
+    q, k and v as they are then; launches of one plan must not overlap (one
+    stream, or ordered).  ``close()`` (or leaving a ``with`` block) releases
+    the graph and its workspace."""
 
-    def __init__(self, q, k, v, softmax_scale: float | None = None, out=None, lse=None):
+    def __init__(self, q, k, v, softmax_scale: float | None = None, out=None, lse=None, smooth_k: bool = False,
+                 fused_q: bool = False):
         lib = load_library()
         for name, t in (("q", q), ("k", k), ("v", v)):
             if not isinstance(t, torch.Tensor) or t.dtype != torch.bfloat16 or not t.is_cuda \
@@ -283,8 +290,10 @@ class Plan:
         self._lib = lib
         self._h = ctypes.c_void_p(0)
         with torch.cuda.device(q.device):
-            _check(lib.sage_plan_create(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse) if lse is not None else None,
-                                        B, Sq, k.shape[1], H, D, float(softmax_scale), ctypes.byref(self._h)))
+            flags = (PLAN_SMOOTH_K if smooth_k else 0) | (PLAN_FUSED_Q if fused_q else 0)
+            _check(lib.sage_plan_create_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(out),
+                                           _ptr(lse) if lse is not None else None, B, Sq, k.shape[1], H, D,
+                                           float(softmax_scale), flags, ctypes.byref(self._h)))
 
     def launch(self):
         if not self._h:

@@ -174,3 +174,24 @@ def test_plan_checks_its_arguments_on_the_host(lib):
     assert b"lse" in lib.sage_last_error()
     assert lib.sage_plan_launch(None, None) == INVALID
     assert lib.sage_plan_destroy(None) == OK
+
+
+def test_plan_options_are_checked_on_the_host(lib):
+    """sage_plan_create_ex records the K-smoothing or fused-Q call: unknown
+    bits and both options at once are UNSUPPORTED, either option with
+    Sq != Skv or an lse buffer is INVALID_ARG, all before any CUDA call and
+    with *plan left NULL."""
+    args = (P(FAKE), P(FAKE), P(FAKE), P(FAKE), None)
+    for flags, want in ((4, UNSUPPORTED), (qad.PLAN_SMOOTH_K | qad.PLAN_FUSED_Q, UNSUPPORTED)):
+        h = ctypes.c_void_p(FAKE)
+        assert lib.sage_plan_create_ex(*args, 1, 256, 256, 2, 128, 0.1, flags, ctypes.byref(h)) == want
+        assert h.value is None
+    for flags in (qad.PLAN_SMOOTH_K, qad.PLAN_FUSED_Q):
+        h = ctypes.c_void_p(FAKE)
+        assert lib.sage_plan_create_ex(*args, 1, 256, 300, 2, 128, 0.1, flags, ctypes.byref(h)) == INVALID
+        assert b"self-attention" in lib.sage_last_error()
+        assert h.value is None
+        assert lib.sage_plan_create_ex(P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE), 1, 256, 256, 2, 128, 0.1, flags,
+                                       ctypes.byref(h)) == INVALID
+        assert lib.sage_plan_create_ex(*args, 1, 256, 256, 2, 64, 0.1, flags, ctypes.byref(h)) == UNSUPPORTED
+    assert lib.sage_plan_create_ex(*args, 1, 256, 256, 2, 128, 0.1, 0, None) == INVALID

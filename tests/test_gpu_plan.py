@@ -144,6 +144,28 @@ def test_plan_on_a_side_stream_and_after_close():
         plan.launch()
 
 
+@pytest.mark.parametrize("option", ["smooth_k", "fused_q"])
+@pytest.mark.parametrize("B,S,H,recipe,seed", [(1, 300, 2, "k_channel_offset", 320),
+                                               (2, 129, 3, "qk_outlier_channels", 321)])
+def test_plan_variants_replay_their_direct_calls(option, B, S, H, recipe, seed):
+    """A plan made with smooth_k (fused_q) replays sage_attn_fwd_smooth_k
+    (sage_attn_fwd_fused_q) bit for bit; the smooth-K and fused-Q tests pin
+    those calls to the oracle.  On a K-offset input smoothing changes the
+    output, so the option is seen to take effect."""
+    import quantized_attention_diffusion_gb300 as qad
+    q, k, v = [t.cuda() for t in make_qkv(B, S, H, recipe=recipe, seed=seed)]
+    ref = qad.attn_fwd(q, k, v, **{option: True})
+    plain = qad.attn_fwd(q, k, v)
+    with qad.Plan(q, k, v, **{option: True}) as plan:
+        for _ in range(2):
+            out = plan.launch()
+        torch.cuda.synchronize()
+        assert qad.sync_status() == 0
+        assert _same_bits(out, ref)
+    if option == "smooth_k" and recipe == "k_channel_offset":
+        assert not _same_bits(ref, plain)
+
+
 def test_out_must_be_32_byte_aligned():
     """The attention kernel writes output rows as 32-byte vectors: an `out`
     that is only 16-byte aligned is rejected on the host, before any launch,
