@@ -735,7 +735,9 @@ cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream) {
 
 cudaError_t load_attention_kernels() {
   cudaFuncAttributes fa;
-  return cudaFuncGetAttributes(&fa, sage_attn_kernel<false, false>);
+  cudaError_t e = cudaFuncGetAttributes(&fa, sage_attn_kernel<false, false>);
+  if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, sage_attn_kernel<false, true>);
+  return e;
 }
 
 cudaError_t read_and_clear_device_error(int* code, cudaStream_t stream) {

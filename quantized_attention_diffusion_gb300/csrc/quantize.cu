@@ -530,10 +530,16 @@ cudaError_t launch_qkv_quantize(const QKQuantArgs<CodeT>& a, const uint16_t* v, 
   return launch_dependent(v_encode_kernel, heads_grid(S_pad / 128, a.BH), dim3(kVEncThreads), stream, v, a.S[1],
                           a.H, a.BH, S_pad, static_cast<const uint32_t*>(amax_bits), vt, v_scale);
 }
+
+// Every kernel a quantise-then-attend call launches, K smoothing included.
 cudaError_t load_quantize_kernels() {
   cudaFuncAttributes fa;
-  cudaError_t e = cudaFuncGetAttributes(&fa, qkv_pass1_kernel<__half, false>);
+  cudaError_t e = cudaFuncGetAttributes(&fa, zero_words_kernel);
+  if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, qkv_pass1_kernel<__half, false>);
+  if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, qkv_pass1_kernel<__half, true>);
   if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, v_encode_kernel);
+  if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, k_sum_kernel);
+  if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, k_mean_kernel);
   return e;
 }
 

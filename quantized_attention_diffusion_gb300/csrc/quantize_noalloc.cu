@@ -106,8 +106,8 @@ extern "C" sage_status sage_quantize_qkv_noalloc(const void* q, const void* k, c
   qa.BH = B * H;
   qa.H = H;
   qa.set_lengths(S, S);
-  // launch_qkv_quantize zeroes the maxima (cudaMemsetAsync, no allocation)
-  // before reducing into them, so the previous call's contents never leak.
+  // launch_qkv_quantize zeroes the maxima (a kernel, no allocation) before
+  // reducing into them, so the previous call's contents never leak.
   cudaError_t e = sage::launch_qkv_quantize<int8_t>(qa, static_cast<const uint16_t*>(v), scratch, vt_fp8, v_scale, st);
   if (e != cudaSuccess) {
     sage::set_last_error("quantisation launch failed: %s", cudaGetErrorString(e));

@@ -38,11 +38,12 @@ struct QKQuantArgs {
   }
 };
 
-// The quantisation of Q, K and V, in two launches: Q/K codes together with
-// the per-channel V maxima (amax_bits [B*H*128] scratch, zeroed here), then
-// the E4M3 V^T codes and scales (vt [B, H, 128, S_pad], v_scale [B, H, 128]).
-// V has the K length a.S[1].  With v == nullptr only the Q/K codes are made
-// (one launch; amax_bits, vt and v_scale unused).
+// The quantisation of Q, K and V, in three launches: the zeroing of the
+// per-channel V maxima (amax_bits [B*H*128] scratch), the Q/K codes together
+// with those maxima, then the E4M3 V^T codes and scales (vt [B, H, 128,
+// S_pad], v_scale [B, H, 128]).  V has the K length a.S[1].  With
+// v == nullptr only the Q/K codes are made (one launch; amax_bits, vt and
+// v_scale unused).
 template <typename CodeT>
 cudaError_t launch_qkv_quantize(const QKQuantArgs<CodeT>& a, const uint16_t* v, uint32_t* amax_bits, uint8_t* vt,
                                 float* v_scale, cudaStream_t stream);
@@ -78,8 +79,8 @@ struct AttnArgs {
 // Encodes the three TMA maps and launches the fused attention kernel.
 cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream);
 
-// Load the kernels the default attention path launches (the two quantisation
-// kernels and the attention kernel) into the current context, so that a
+// Load every kernel a quantise-then-attend call can launch (K smoothing and
+// the fused-Q attention kernel included) into the current context, so that a
 // stream capture that launches them does not have to load a module.
 cudaError_t load_attention_kernels();
 cudaError_t load_quantize_kernels();

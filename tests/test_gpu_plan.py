@@ -9,6 +9,11 @@ inputs as they are at that point of the stream, allocates nothing from the
 library's pool, and failures injected on the host during creation leave the
 library usable.
 """
+import json
+import os
+import subprocess
+import sys
+
 import numpy as np
 import pytest
 import torch
@@ -184,3 +189,36 @@ def test_out_must_be_32_byte_aligned():
     assert ei.value.status == 3
     torch.cuda.synchronize()
     assert bool((buf == 0).all())                                         # nothing was written
+
+
+_FIRST_CALLS_ARE_PLANS = r"""
+import json, sys
+import torch
+sys.path.insert(0, sys.argv[1])
+import quantized_attention_diffusion_gb300 as qad
+from quantized_attention_diffusion_gb300.workloads import make_qkv
+q, k, v = [t.cuda() for t in make_qkv(1, 300, 2, recipe="k_channel_offset", seed=330)]
+outs = {}
+for name, opts in (("smooth_k", {"smooth_k": True}), ("fused_q", {"fused_q": True}), ("plain", {})):
+    with qad.Plan(q, k, v, **opts) as plan:               # before any direct call of the library
+        outs[name] = plan.launch().clone()
+torch.cuda.synchronize()
+status = qad.sync_status()
+same = {name: torch.equal(outs[name].view(torch.int16), qad.attn_fwd(q, k, v, **opts).view(torch.int16))
+        for name, opts in (("smooth_k", {"smooth_k": True}), ("fused_q", {"fused_q": True}), ("plain", {}))}
+torch.cuda.synchronize()
+print(json.dumps({"status": status, "same": same}))
+"""
+
+
+def test_plans_recorded_before_any_direct_call():
+    """In a fresh process with lazy module loading, plans are the library's
+    first calls: creation loads every kernel it records before the capture,
+    and each plan's replay equals the direct call made afterwards."""
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, CUDA_MODULE_LOADING="LAZY")
+    res = subprocess.run([sys.executable, "-c", _FIRST_CALLS_ARE_PLANS, root], capture_output=True, text=True,
+                         timeout=600, env=env)
+    assert res.returncode == 0, res.stderr[-2000:]
+    rec = json.loads(res.stdout.strip().splitlines()[-1])
+    assert rec["status"] == 0 and all(rec["same"].values()), rec
