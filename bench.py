@@ -308,6 +308,27 @@ def attention_traffic():
 
 # -------------------------------------------------------- oracle timing --
 
+def cpu_model() -> str:
+    """The host CPU's model name (x86 /proc/cpuinfo, else lscpu, which also
+    names Arm cores), for the oracle's timing record."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    import platform
+    return platform.machine() or "unknown"
+
+
 def oracle_sample(w, q, k, v, seconds: float, steps: int = 1):
     """Time the CPU oracle on a bounded sample: one (batch, head) of the
     workload, quantised whole, and as many of its query rows as fit in
@@ -542,7 +563,7 @@ def run_ours(args, group, local):
     }
     if group.rank == 0 and group.world == 1 and not args.no_cpu_baseline:
         tops, sample, cores, _, _ = oracle_sample(w, *cpu_sample, args.cpu_seconds)
-        line["cpu_baseline"] = {"value": round(tops, 6), "unit": UNIT, "cores": cores,
+        line["cpu_baseline"] = {"value": round(tops, 6), "unit": UNIT, "cores": cores, "cpu": cpu_model(),
                                 "kind": "oracle", "sample": sample}
     return line
 
@@ -569,7 +590,7 @@ def run_reference(args):
         "config": {"workload": w.name, "B": w.B, "S": w.S, "Skv": w.skv, "H": w.H, "D": w.D, "recipe": w.recipe,
                    "seed": w.seed, "softmax_scale": w.softmax_scale,
                    "path": "CPU oracle (plain C, OpenMP) on a bounded sample per step"},
-        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": cores, "kind": "oracle",
+        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": cores, "cpu": cpu_model(), "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
