@@ -515,6 +515,12 @@ def run_ours(args, group, local):
         clock_peak = 4.0 / 3.0 * FP16_FLOP_PER_CLK_SM * N_SMS * clocks["sm_mhz"] * 1e6 / 1e12
     exps = w.B * w.H * w.S * w.skv
     xu_ms = exps / (EX2_PER_CLK_SM * N_SMS * (clocks.get("sm_mhz") or MAX_SM_MHZ) * 1e6) * 1e3
+    # The quantisation pass: 3 B per element of each tensor it quantises
+    # (2 B of bf16 read, 1 B of code written); with fused Q, Q is quantised
+    # inside the attention kernel, and K smoothing reads K once more.
+    e_q, e_kv = w.B * w.S * w.H * w.D, w.B * w.skv * w.H * w.D
+    q_bytes = (0 if args.fused_q else 3 * e_q) + 6 * e_kv + (2 * e_kv if args.smooth_k else 0)
+    quant_ms = ms_max / K - attn_ms_max
     line = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -558,6 +564,14 @@ def run_ours(args, group, local):
                                  "frac": round(xu_ms / attn_ms_max, 4),
                                  "basis": f"one ex2.approx per score element, {N_SMS} SMs x {EX2_PER_CLK_SM} "
                                           f"per clock at the sampled SM clock"}},
+        },
+        "quantise": {
+            "ms_per_step": round(quant_ms, 4), "algorithmic_bytes": q_bytes,
+            "achieved_gbs": round(q_bytes / (quant_ms * 1e-3) / 1e9, 1) if quant_ms > 0 else None,
+            "peak_gbs": round(hbm, 1),
+            "frac": round(q_bytes / (quant_ms * 1e-3) / 1e9 / hbm, 4) if quant_ms > 0 else None,
+            "note": "step time outside the attention kernel: the quantisation launches and the gaps between "
+                    "launches; bytes are the pass's algorithmic 3 per element of each tensor it quantises",
         },
         "clocks": clocks,
     }
