@@ -72,6 +72,28 @@ def test_smooth_k_attention_matches_oracle(B, S, H, recipe, seed):
     assert_within_two_pass_bound(got, quant, S, scale, rows, ties, f"smooth B{B} S{S} H{H} vs two-pass")
 
 
+def test_smooth_k_means_exact_over_wide_magnitudes():
+    """Channels 0-63 of K ordinary N(0,1) values (each thread's fp32 partial
+    sums are exact and kept), channels 64-127 spread log-uniformly over
+    [2^-33, 2^3) with random signs (fp32 additions round, so those threads
+    redo their slices in 2^-40 fixed point); 1000 tokens, four slices, the
+    last one partial.  Every channel's sum stays below 2^13, where the mean
+    is the exactly rounded one: the means and the K codes equal the
+    oracle's bit for bit."""
+    g = torch.Generator().manual_seed(340)
+    B, S, H = 1, 1000, 2
+    q = torch.randn((B, S, H, 128), generator=g).to(torch.bfloat16)
+    v = torch.randn((B, S, H, 128), generator=g).to(torch.bfloat16)
+    mag = torch.exp2(torch.rand((B, S, H, 64), generator=g, dtype=torch.float64) * 36.0 - 33.0)
+    sign = torch.where(torch.rand((B, S, H, 64), generator=g) < 0.5, -1.0, 1.0).to(torch.float64)
+    k = torch.cat([torch.randn((B, S, H, 64), generator=g, dtype=torch.float64), mag * sign], dim=-1)
+    k = k.to(torch.bfloat16)
+    ak = k.float().abs()
+    assert bool(((ak == 0) | ((ak >= 2.0 ** -33) & (ak < 2.0 ** 22))).all())
+    assert float(k.double().sum(dim=1).abs().max()) < 2.0 ** 13
+    _check_quant((q, k, v), [bf16_bits(t) for t in (q, k, v)])
+
+
 def test_exact_channel_offset_is_removed_on_gpu():
     """Zero-mean integer keys plus an exact per-channel offset: smoothed
     attention equals plain attention on the offset-free keys bit for bit."""
