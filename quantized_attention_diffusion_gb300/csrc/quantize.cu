@@ -281,13 +281,14 @@ __device__ __forceinline__ long long bf16_fixed40(uint32_t h) {
 // depend on the order of the slices, and it equals the exact sum for the
 // magnitudes bf16_fixed40 keeps exactly.
 //
-// A thread first adds its 16 tokens of 8 channels in fp32 and keeps those
-// sums only where they are provably exact in that grid: every value zero or
-// in [2^-33, 2^22) (so a whole number of 2^-40 units, as bf16_fixed40 counts
-// it), every addition exact (the TwoSum rounding error (a - (s - b')) +
-// (x - b') with b' = s - a is zero) and the partial sum below 2^23 (so times
-// 2^40 it is an int64).  Then sum * 2^40 is the integer bf16_fixed40 would
-// have accumulated; otherwise the thread redoes its slice with it.
+// A thread first adds its 16 tokens of 8 channels in fp32 and keeps a
+// channel's sum only where it is provably exact in that grid: every value
+// zero or in [2^-33, 2^22) (so a whole number of 2^-40 units, as
+// bf16_fixed40 counts it), every addition exact (the TwoSum rounding error
+// (a - (s - b')) + (x - b') with b' = s - a is zero) and the partial sum
+// below 2^23 (so times 2^40 it is an int64).  Then sum * 2^40 is the integer
+// bf16_fixed40 would have accumulated; a channel that fails redoes its 16
+// values with bf16_fixed40.
 __global__ void __launch_bounds__(256) k_sum_kernel(const uint16_t* __restrict__ k, int S, int H, int BH,
                                                     unsigned long long* __restrict__ sums) {
   __shared__ long long part[16][kHeadDim];
@@ -300,42 +301,41 @@ __global__ void __launch_bounds__(256) k_sum_kernel(const uint16_t* __restrict__
   const int s1 = min(S, s0 + kVRowsPerCta);
   const size_t tok_stride = static_cast<size_t>(H) * kHeadDim;
   const uint16_t* src = k + (static_cast<size_t>(b) * S * H + h) * kHeadDim + c8;
+  uint4 buf[kVRowsPerCta / 16];   // all of this thread's tokens in flight (zeros past the slice)
+#pragma unroll
+  for (int u = 0; u < kVRowsPerCta / 16; ++u) {
+    const int s = s0 + r + 16 * u;
+    buf[u] = s < s1 ? __ldg(reinterpret_cast<const uint4*>(src + static_cast<size_t>(s) * tok_stride))
+                    : make_uint4(0u, 0u, 0u, 0u);
+  }
   float f[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
-  bool exact = true;
-  for (int s = s0 + r; s < s1; s += 16) {
-    const uint4 q = __ldg(reinterpret_cast<const uint4*>(src + static_cast<size_t>(s) * tok_stride));
-    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+  uint32_t inexact = 0;   // bit i: channel c8 + i takes the fixed-point path
+#pragma unroll
+  for (int u = 0; u < kVRowsPerCta / 16; ++u) {
+    const uint32_t w[4] = {buf[u].x, buf[u].y, buf[u].z, buf[u].w};
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const float x = __uint_as_float((i & 1) ? (w[i >> 1] & 0xFFFF0000u) : (w[i >> 1] << 16));
       const float ax = fabsf(x);
       const float a = f[i], sum = a + x, bp = sum - a;
-      exact &= ((ax >= 0x1p-33f) & (ax < 0x1p22f)) | (ax == 0.0f);
-      exact &= (a - (sum - bp)) + (x - bp) == 0.0f;
+      const bool ok = (((ax >= 0x1p-33f) & (ax < 0x1p22f)) | (ax == 0.0f)) & ((a - (sum - bp)) + (x - bp) == 0.0f);
+      inexact |= ok ? 0u : (1u << i);
       f[i] = sum;
     }
   }
-  long long m[8];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) exact &= fabsf(f[i]) < 0x1p23f;
-  if (exact) {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) m[i] = __float2ll_rz(f[i] * 0x1p40f);
-  } else {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) m[i] = 0;
-    for (int s = s0 + r; s < s1; s += 16) {
-      const uint4 q = __ldg(reinterpret_cast<const uint4*>(src + static_cast<size_t>(s) * tok_stride));
-      const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        m[2 * i] += bf16_fixed40(w[i] & 0xFFFFu);
-        m[2 * i + 1] += bf16_fixed40(w[i] >> 16);
-      }
-    }
+  for (int i = 0; i < 8; ++i) {
+    if (!(fabsf(f[i]) < 0x1p23f)) inexact |= 1u << i;
+    part[r][c8 + i] = __float2ll_rz(f[i] * 0x1p40f);
   }
-#pragma unroll
-  for (int i = 0; i < 8; ++i) part[r][c8 + i] = m[i];
+  // The channels whose fp32 sum is not provably exact, again in fixed point.
+#pragma unroll 1
+  for (int i = 0; i < 8; ++i) {
+    if (!(inexact & (1u << i))) continue;
+    long long acc = 0;
+    for (int s = s0 + r; s < s1; s += 16) acc += bf16_fixed40(src[static_cast<size_t>(s) * tok_stride + i]);
+    part[r][c8 + i] = acc;
+  }
   __syncthreads();
   if (t < kHeadDim) {
     long long mm = part[0][t];
