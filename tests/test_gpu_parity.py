@@ -226,6 +226,24 @@ def test_single_token_returns_v():
     assert (out - v).abs().max().item() <= 1e-2 * v.abs().max().item()
 
 
+@pytest.mark.parametrize("which", [0, 1], ids=["zero_q", "zero_k"])
+def test_zero_q_or_k_gives_uniform_attention(which):
+    """With Q (or K) all zero every block scale and code is 0, so every score
+    is 0 and every P~ is 448: each output row is the mean of the dequantised
+    V over the keys, the same for every query (the zero-scale path through
+    the attention kernel).  Element-wise against the oracle, and every row
+    equal."""
+    import quantized_attention_diffusion_gb300 as qad
+    from quantized_attention_diffusion_gb300.workloads import bf16_bits
+    qkv, _ = gen(2, 300, 2, "normal", 12)
+    qkv = list(qkv)
+    qkv[which] = torch.zeros_like(qkv[which])
+    bits = [bf16_bits(t) for t in qkv]
+    out = bf16_out_to_f32(qad.attn_fwd(*[t.cuda() for t in qkv]))
+    _check_output(out, *bits, default_scale())
+    assert (out == out[:, :1]).all()
+
+
 def test_heads_are_independent_on_gpu():
     import quantized_attention_diffusion_gb300 as qad
     qkv, _ = gen(2, 260, 3, "normal", 11)
